@@ -1,0 +1,37 @@
+"""Algorithmic work of one attention forward, for throughput reporting.
+
+FLOPs: each of the two products costs 2*d FLOPs per visible (query, key)
+pair per head, 4*d in all ("Attention and Its Computational Cost",
+section "What is being computed"); a causal mask keeps, for row i of T_q
+rows against T_kv keys, the keys j <= i + T_kv - T_q.
+
+Bytes: what the method must move at minimum -- Q, K, V read once, O written
+once (16-bit) and the fp32 logsumexp written once. The score and
+probability matrices are not counted: they never leave the chip.
+"""
+
+from __future__ import annotations
+
+
+def visible_pairs(T_q: int, T_kv: int, causal: bool) -> int:
+    if not causal:
+        return T_q * T_kv
+    # rows i = 0..T_q-1 each see T_kv - T_q + i + 1 keys
+    first = T_kv - T_q + 1
+    return T_q * first + T_q * (T_q - 1) // 2
+
+
+def flops(B: int, h: int, T_q: int, T_kv: int, d: int, causal: bool) -> int:
+    return 4 * d * B * h * visible_pairs(T_q, T_kv, causal)
+
+
+def min_bytes(B: int, h: int, T_q: int, T_kv: int, d: int, elem: int = 2) -> int:
+    qo = 2 * B * h * T_q * d * elem
+    kv = 2 * B * h * T_kv * d * elem
+    lse = B * h * T_q * 4
+    return qo + kv + lse
+
+
+def kv_cache_bytes(B: int, h: int, T_kv: int, d: int, elem: int = 2) -> int:
+    """The bytes a decode step must stream: every cached key and value."""
+    return 2 * B * h * T_kv * d * elem

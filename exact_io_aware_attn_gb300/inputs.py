@@ -1,0 +1,92 @@
+"""Seeded synthetic inputs and the workload table.
+
+This module holds no attention arithmetic: it only draws Q, K and V from a
+seeded generator and names the workloads. Both the GPU path (tests, bench)
+and the oracle's callers use it, so the two sides see the very same 16-bit
+tensors.
+
+Recipe: torch.Generator("cpu").manual_seed(seed); torch.randn in float32 for
+q, then k, then v, each of shape [B, h, T, d]; multiplied by `mult`
+(0.5 for the very-long workload, 1 elsewhere); then cast to the 16-bit
+dtype (round to nearest even). The shapes, dtypes and masks follow the
+pages' GPT-2 head geometry (12 heads of width 64, "Attention and Its
+Computational Cost", section "What the numbers do not show") and the
+sequence lengths they measure (up to 16,384 tokens).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+F16 = 0
+BF16 = 1
+
+_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
+_NAME = {F16: "f16", BF16: "bf16"}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    h: int
+    T_q: int
+    T_kv: int
+    d: int
+    dtype: int          # F16 or BF16
+    causal: bool
+    mult: float = 1.0
+    seed: int = 0
+
+    @property
+    def torch_dtype(self):
+        return _TORCH_DTYPE[self.dtype]
+
+    @property
+    def dtype_name(self) -> str:
+        return _NAME[self.dtype]
+
+    @property
+    def scale(self) -> float:
+        return self.d ** -0.5
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "h": self.h,
+                "T_q": self.T_q, "T_kv": self.T_kv, "d": self.d,
+                "dtype": self.dtype_name, "causal": self.causal,
+                "input_scale": self.mult, "seed": self.seed}
+
+
+# The five workloads (seven runs) the kernels are checked and measured on.
+TINY = Workload("tiny_noncausal_B1_h2_T256_d64_f16", 1, 2, 256, 256, 64, F16, False)
+GPT2_PREFILL = Workload("gpt2_causal_prefill_B8_h12_T1024_d64_bf16", 8, 12, 1024, 1024, 64, BF16, True)
+LONG_4K = Workload("long_causal_prefill_B1_h16_T4096_d64_bf16", 1, 16, 4096, 4096, 64, BF16, True)
+LONG_8K = Workload("long_causal_prefill_B1_h16_T8192_d64_bf16", 1, 16, 8192, 8192, 64, BF16, True)
+LONG_8K_D128 = Workload("long_causal_prefill_B1_h16_T8192_d128_bf16", 1, 16, 8192, 8192, 128, BF16, True)
+VERY_LONG = Workload("very_long_causal_prefill_B1_h12_T16384_d64_f16_x0.5", 1, 12, 16384, 16384, 64, F16, True, mult=0.5)
+DECODE = Workload("decode_B32_h12_Tkv16384_d64_bf16", 32, 12, 1, 16384, 64, BF16, False)
+
+WORKLOADS = [TINY, GPT2_PREFILL, LONG_4K, LONG_8K, LONG_8K_D128, VERY_LONG, DECODE]
+
+
+def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu"):
+    """Draw q [B,h,T_q,d], k and v [B,h,T_kv,d] as 16-bit tensors.
+
+    The draw happens on the CPU generator (so every machine gets the same
+    values) and the result is then moved to `device`.
+    """
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    out = []
+    for t in (T_q, T_kv, T_kv):
+        x = torch.randn((B, h, t, d), generator=gen, dtype=torch.float32)
+        if mult != 1.0:
+            x.mul_(mult)
+        out.append(x.to(_TORCH_DTYPE[dtype]).to(device))
+    return tuple(out)
+
+
+def make_workload(w: Workload, device="cpu"):
+    return make_qkv(w.B, w.h, w.T_q, w.T_kv, w.d, w.dtype, w.mult, w.seed, device)

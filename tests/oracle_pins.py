@@ -1,0 +1,271 @@
+"""Pins for the oracle: checks against things other than the oracle itself.
+
+Each check takes an implementation bundle (the real oracle, or a mutant with
+a planted mistake) and returns a list of failure messages (empty = pinned).
+The checks draw on:
+
+* values the pages print (tests/golden/worked_example.json),
+* a pure-Python brute force (no max subtraction, math.fsum) on tiny inputs,
+* a library routine (torch scaled_dot_product_attention / logsumexp in
+  float64 on the CPU),
+* closed forms (one key, all-zero keys, causal row 0, one dominant key),
+* invariants (key shift, joint key/value permutation, affine maps of V,
+  folding a factor of q into the scale),
+* exactness of the blocking and of the split merge (block sizes 1..n,
+  partition counts 1..n+3).
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+import types
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def real_oracle():
+    import oracle
+    return types.SimpleNamespace(
+        standard_attention=oracle.standard_attention,
+        standard_attention_row=oracle.standard_attention_row,
+        online_attention=oracle.online_attention,
+        online_softmax_states=oracle.online_softmax_states,
+        split_partials=oracle.split_partials,
+        merge_partials=oracle.merge_partials,
+        split_kv_attention=oracle.split_kv_attention,
+    )
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, rtol=1e-12, atol=1e-12):
+    return np.allclose(a, b, rtol=rtol, atol=atol)
+
+
+# --------------------------------------------------------------------------
+def check_worked_example(impl):
+    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+        ex = json.load(f)
+    fails = []
+    states = impl.online_softmax_states(ex["scores"], ex["block"])
+    m1, l1 = states[0]
+    if m1 != ex["after_block_1"]["m"]:
+        fails.append(f"block-1 max {m1} != {ex['after_block_1']['m']}")
+    if round(l1, ex["after_block_1"]["printed_decimals"]) != ex["after_block_1"]["l"]:
+        fails.append(f"block-1 sum {l1:.6f} does not print as {ex['after_block_1']['l']}")
+    m2, l2 = states[1]
+    full_max = max(ex["scores"])
+    full_sum = math.fsum(math.exp(s - full_max) for s in ex["scores"])
+    if m2 != ex["after_block_2"]["m"] or m2 != full_max:
+        fails.append(f"block-2 max {m2} != {full_max}")
+    if not math.isclose(l2, full_sum, rel_tol=1e-14):
+        fails.append(f"block-2 sum {l2!r} != full-row sum {full_sum!r}")
+    return fails
+
+
+def check_blockwise_equals_full(impl):
+    fails = []
+    rng = _rng(1)
+    for n, d in ((1, 4), (7, 8), (33, 16)):
+        for trial in range(2):
+            q = rng.standard_normal(d) * 2.0
+            k = rng.standard_normal((n, d)) * 2.0
+            v = rng.standard_normal((n, d + 1))
+            o_ref, _ = impl.standard_attention_row(q, k, v)
+            for block in range(1, n + 2):
+                o = impl.online_attention(q, k, v, block)
+                if not _close(o, o_ref, rtol=1e-11, atol=1e-12):
+                    fails.append(f"online(block={block}) != standard at n={n}")
+                    break
+    return fails
+
+
+def _brute(q, k, v, scale, causal):
+    """Pure-Python attention: weights exp(scale q.k) summed with fsum."""
+    t_q, t_kv = len(q), len(k)
+    out, lse = [], []
+    for i in range(t_q):
+        w = []
+        for j in range(t_kv):
+            if causal and j > i + (t_kv - t_q):
+                w.append(0.0)
+            else:
+                dot = math.fsum(q[i][c] * k[j][c] for c in range(len(q[i])))
+                w.append(math.exp(scale * dot))
+        z = math.fsum(w)
+        out.append([math.fsum(w[j] * v[j][c] for j in range(t_kv)) / z
+                    for c in range(len(v[0]))])
+        lse.append(math.log(z))
+    return np.array(out), np.array(lse)
+
+
+def check_bruteforce(impl):
+    fails = []
+    rng = _rng(2)
+    for t_q, t_kv, d in ((1, 1, 3), (3, 5, 4), (5, 5, 4), (2, 8, 3), (8, 8, 5)):
+        q = rng.standard_normal((t_q, d))
+        k = rng.standard_normal((t_kv, d))
+        v = rng.standard_normal((t_kv, d))
+        for causal in (False, True):
+            scale = 0.7
+            o_b, l_b = _brute(q.tolist(), k.tolist(), v.tolist(), scale, causal)
+            o, l = impl.standard_attention(q, k, v, scale=scale, causal=causal)
+            if not (_close(o, o_b, rtol=1e-12, atol=1e-13)
+                    and _close(l, l_b, rtol=1e-12, atol=1e-13)):
+                fails.append(f"brute force mismatch t_q={t_q} t_kv={t_kv} causal={causal}")
+    return fails
+
+
+def check_library(impl):
+    import torch
+    import torch.nn.functional as F
+    fails = []
+    rng = _rng(3)
+    for (b, h, t_q, t_kv, d) in ((1, 2, 16, 16, 8), (2, 1, 5, 19, 16), (1, 3, 1, 40, 8)):
+        q = rng.standard_normal((b, h, t_q, d))
+        k = rng.standard_normal((b, h, t_kv, d))
+        v = rng.standard_normal((b, h, t_kv, d))
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        for causal in (False, True):
+            if causal:
+                # bottom-right alignment, built independently of the oracle
+                mask = torch.ones(t_q, t_kv, dtype=torch.bool).tril(diagonal=t_kv - t_q)
+            else:
+                mask = None
+            o_lib = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask).numpy()
+            s = (tq @ tk.transpose(-1, -2)) / math.sqrt(d)
+            if mask is not None:
+                s = s.masked_fill(~mask, float("-inf"))
+            lse_lib = torch.logsumexp(s, dim=-1).numpy()
+            o, lse = impl.standard_attention(q, k, v, causal=causal)
+            if not (_close(o, o_lib, rtol=1e-10, atol=1e-12)
+                    and _close(lse, lse_lib, rtol=1e-12, atol=1e-12)):
+                fails.append(f"library mismatch shape={(b, h, t_q, t_kv, d)} causal={causal}")
+    return fails
+
+
+def check_closed_forms(impl):
+    fails = []
+    rng = _rng(4)
+    d = 6
+    # one key: O = V, lse = scale q.k
+    q = rng.standard_normal((3, d))
+    k = rng.standard_normal((1, d))
+    v = rng.standard_normal((1, d))
+    o, lse = impl.standard_attention(q, k, v, scale=0.5)
+    if not (_close(o, np.repeat(v, 3, axis=0)) and _close(lse, 0.5 * (q @ k[0]))):
+        fails.append("T_kv = 1 closed form")
+    # all-zero keys: uniform weights, O = mean(V), lse = ln T_kv
+    k0 = np.zeros((9, d))
+    v9 = rng.standard_normal((9, d))
+    o, lse = impl.standard_attention(q, k0, v9)
+    if not (_close(o, np.repeat(v9.mean(axis=0, keepdims=True), 3, axis=0))
+            and _close(lse, np.full(3, math.log(9)))):
+        fails.append("K = 0 closed form")
+    # causal, square: row 0 sees only key 0
+    q5 = rng.standard_normal((5, d))
+    k5 = rng.standard_normal((5, d))
+    v5 = rng.standard_normal((5, d))
+    o, lse = impl.standard_attention(q5, k5, v5, scale=0.3, causal=True)
+    if not (_close(o[0], v5[0]) and math.isclose(lse[0], 0.3 * float(q5[0] @ k5[0]),
+                                                  rel_tol=1e-12, abs_tol=1e-12)):
+        fails.append("causal row 0 closed form")
+    # causal, one query against a cache: sees every key (equals non-causal)
+    o_c, l_c = impl.standard_attention(q5[:1], k5, v5, causal=True)
+    o_n, l_n = impl.standard_attention(q5[:1], k5, v5, causal=False)
+    if not (_close(o_c, o_n) and _close(l_c, l_n)):
+        fails.append("one causal query must see the whole cache")
+    # last causal row of a square problem sees every key
+    o_l, _ = impl.standard_attention(q5[4:5], k5, v5, scale=0.3)
+    if not _close(o[4], o_l[0]):
+        fails.append("causal last row must equal the unmasked row")
+    # one dominant key: weight -> 1
+    kd = np.zeros((4, 2))
+    kd[2] = [100.0, 0.0]
+    qd = np.array([[10.0, 0.0]])
+    vd = np.arange(8.0).reshape(4, 2)
+    o, lse = impl.standard_attention(qd, kd, vd, scale=1.0)
+    if not (_close(o[0], vd[2]) and math.isclose(lse[0], 1000.0, rel_tol=1e-12)):
+        fails.append("dominant key closed form")
+    return fails
+
+
+def check_invariants(impl):
+    fails = []
+    rng = _rng(5)
+    t_q, t_kv, d = 6, 11, 8
+    q = rng.standard_normal((t_q, d))
+    k = rng.standard_normal((t_kv, d))
+    v = rng.standard_normal((t_kv, d))
+    s = 0.4
+    for causal in (False, True):
+        o, lse = impl.standard_attention(q, k, v, scale=s, causal=causal)
+        u = rng.standard_normal(d)
+        o2, lse2 = impl.standard_attention(q, k + u, v, scale=s, causal=causal)
+        if not (_close(o2, o, rtol=1e-10, atol=1e-11)
+                and _close(lse2, lse + s * (q @ u), rtol=1e-10, atol=1e-11)):
+            fails.append(f"key shift invariance (causal={causal})")
+        a, b = -1.7, rng.standard_normal(d)
+        o3, lse3 = impl.standard_attention(q, k, a * v + b, scale=s, causal=causal)
+        if not (_close(o3, a * o + b, rtol=1e-10, atol=1e-11) and _close(lse3, lse)):
+            fails.append(f"affine map of V (causal={causal})")
+        o4, lse4 = impl.standard_attention(2.5 * q, k, v, scale=s / 2.5, causal=causal)
+        if not (_close(o4, o, rtol=1e-10, atol=1e-11) and _close(lse4, lse, rtol=1e-10)):
+            fails.append(f"scale folding (causal={causal})")
+    perm = rng.permutation(t_kv)
+    o, lse = impl.standard_attention(q, k, v, scale=s)
+    o5, lse5 = impl.standard_attention(q, k[perm], v[perm], scale=s)
+    if not (_close(o5, o, rtol=1e-10, atol=1e-11) and _close(lse5, lse, rtol=1e-12)):
+        fails.append("joint key/value permutation")
+    # rows= selects rows with absolute causal positions
+    rows = np.array([5, 0, 3])
+    o6, lse6 = impl.standard_attention(q, k, v, scale=s, causal=True, rows=rows)
+    o7, lse7 = impl.standard_attention(q, k, v, scale=s, causal=True)
+    if not (_close(o6, o7[rows]) and _close(lse6, lse7[rows])):
+        fails.append("row selection must keep absolute causal positions")
+    return fails
+
+
+def check_split_merge(impl):
+    fails = []
+    rng = _rng(6)
+    for n in (1, 5, 17):
+        d = 8
+        q = rng.standard_normal(d) * 2
+        k = rng.standard_normal((n, d)) * 2
+        v = rng.standard_normal((n, d))
+        o_ref, lse_ref = impl.standard_attention_row(q, k, v)
+        for splits in range(1, n + 4):
+            o, lse = impl.split_kv_attention(q, k, v, splits)
+            if not (_close(o, o_ref, rtol=1e-11, atol=1e-12)
+                    and math.isclose(lse, lse_ref, rel_tol=1e-12, abs_tol=1e-12)):
+                fails.append(f"split merge n={n} splits={splits}")
+                break
+    return fails
+
+
+ALL_CHECKS = [
+    check_worked_example,
+    check_blockwise_equals_full,
+    check_bruteforce,
+    check_library,
+    check_closed_forms,
+    check_invariants,
+    check_split_merge,
+]
+
+
+def run_all(impl):
+    fails = []
+    for check in ALL_CHECKS:
+        try:
+            fails += [f"{check.__name__}: {m}" for m in check(impl)]
+        except Exception as exc:  # a mutant may also crash a check
+            fails.append(f"{check.__name__}: raised {type(exc).__name__}: {exc}")
+    return fails

@@ -1,0 +1,126 @@
+"""Planted mistakes in copies of the oracle must each fail a pin.
+
+This shows that the pins in oracle_pins.py are strong enough: a dropped
+rescale, a wrong sign, an off-by-one mask, a transposed operand, a missing
+normalisation or a wrong default scale in the oracle would not go unnoticed.
+Mutants are built here on the CPU; the real oracle is never modified.
+"""
+
+import math
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle_pins import real_oracle, run_all
+
+
+def _with(**over):
+    base = vars(real_oracle()).copy()
+    base.update(over)
+    ns = types.SimpleNamespace(**base)
+    if "standard_attention" in over and "standard_attention_row" not in over:
+        def row(q, k, v, scale=None, _f=over["standard_attention"]):
+            o, l = _f(np.asarray(q, dtype=np.float64)[None, :], k, v, scale=scale)
+            return o[0], float(l[0])
+        ns.standard_attention_row = row
+    return ns
+
+
+def _std_factory(mask_fn=None, lse_fn=None, transpose_k=False, normalise=True,
+                 default_scale=lambda d: 1.0 / math.sqrt(d)):
+    def std(q, k, v, scale=None, causal=False, rows=None):
+        q = np.asarray(q, dtype=np.float64)
+        k = np.asarray(k, dtype=np.float64)
+        v = np.asarray(v, dtype=np.float64)
+        t_q, t_kv, d = q.shape[-2], k.shape[-2], q.shape[-1]
+        if scale is None:
+            scale = default_scale(d)
+        lead = q.shape[:-2]
+        rws = np.arange(t_q) if rows is None else np.asarray(rows)
+        out = np.empty(lead + (len(rws), v.shape[-1]))
+        lse = np.empty(lead + (len(rws),))
+        for idx in np.ndindex(*lead):
+            kk = k[idx]
+            s = scale * (q[idx][rws] @ (kk if transpose_k else kk.T))
+            if causal:
+                vis = (mask_fn or (lambda i, j, off: j <= i + off))(
+                    rws[:, None], np.arange(t_kv)[None, :], t_kv - t_q)
+                s = np.where(vis, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            p = np.exp(s - m)
+            l = p.sum(axis=1, keepdims=True)
+            o = p @ v[idx]
+            out[idx] = o / l if normalise else o
+            lse[idx] = (lse_fn or (lambda m, l: m + np.log(l)))(m, l)[:, 0]
+        return out, lse
+    return std
+
+
+def _online_factory(rescale=True, sign=1.0):
+    def online(q, k, v, block, scale=None, return_state=False):
+        q = np.asarray(q, dtype=np.float64)
+        if scale is None:
+            scale = 1.0 / math.sqrt(q.shape[0])
+        m, l, o = -np.inf, 0.0, np.zeros(v.shape[1])
+        for st in range(0, k.shape[0], block):
+            s = scale * (k[st:st + block] @ q)
+            m_new = max(m, float(s.max()))
+            alpha = math.exp(sign * (m - m_new)) if rescale else 1.0
+            p = np.exp(s - m_new)
+            l = l * alpha + p.sum()
+            o = o * alpha + p @ v[st:st + block]
+            m = m_new
+        return o / l
+    return online
+
+
+def _states_no_rescale(scores, block):
+    s = np.asarray(scores, dtype=np.float64)
+    m, l, out = -np.inf, 0.0, []
+    for st in range(0, len(s), block):
+        sb = s[st:st + block]
+        m = max(m, float(sb.max()))
+        l = l + float(np.exp(sb - m).sum())
+        out.append((m, l))
+    return out
+
+
+def _merge_unweighted(ms, ls, os_):
+    ms, ls, os_ = (np.asarray(x, dtype=np.float64) for x in (ms, ls, os_))
+    o = os_.sum(axis=0) / ls.sum()
+    return o, float(ms.max() + math.log(ls.sum()))
+
+
+def _split_kv_with(merge):
+    def f(q, k, v, num_splits, scale=None):
+        return merge(*oracle.split_partials(q, k, v, num_splits, scale=scale))
+    return f
+
+
+MUTANTS = {
+    "online_drops_rescale": _with(online_attention=_online_factory(rescale=False)),
+    "online_rescale_wrong_sign": _with(online_attention=_online_factory(sign=-1.0)),
+    "states_drop_rescale": _with(online_softmax_states=_states_no_rescale),
+    "causal_excludes_diagonal": _with(standard_attention=_std_factory(
+        mask_fn=lambda i, j, off: j < i + off)),
+    "causal_top_left": _with(standard_attention=_std_factory(
+        mask_fn=lambda i, j, off: j <= i)),
+    "lse_drops_max": _with(standard_attention=_std_factory(lse_fn=lambda m, l: np.log(l))),
+    "k_not_transposed": _with(standard_attention=_std_factory(transpose_k=True)),
+    "output_not_normalised": _with(standard_attention=_std_factory(normalise=False)),
+    "default_scale_1_over_d": _with(standard_attention=_std_factory(
+        default_scale=lambda d: 1.0 / d)),
+    "merge_ignores_weights": _with(split_kv_attention=_split_kv_with(_merge_unweighted)),
+}
+
+
+def test_real_oracle_passes_every_pin():
+    assert run_all(real_oracle()) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    fails = run_all(MUTANTS[name])
+    assert fails, f"planted mistake '{name}' passed every pin"
