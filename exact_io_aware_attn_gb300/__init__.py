@@ -1,6 +1,20 @@
 """Exact IO-aware attention forward for GB300 (sm_103a).
 
 The compute path is the C-ABI library libattn.so (hand-written CUDA kernels
-under csrc/); this package is its thin ctypes binding plus the seeded input
-generator and the work counter the benchmark uses.
+under csrc/, declared in include/attn.h); this package is its thin ctypes
+binding plus the seeded input generator and the work counter the benchmark
+uses. Importing the package does not load the library; the first call does,
+and fails loudly if it has not been built.
 """
+
+from ._lib import (  # noqa: F401
+    AttnError,
+    abi_version,
+    attn_fwd,
+    decode_num_splits,
+    fwd_raw,
+    get_device_error,
+    last_kernel_name,
+    status_string,
+    workspace_bytes,
+)

@@ -1,0 +1,181 @@
+"""ctypes binding of libattn.so (the C ABI declared in include/attn.h).
+
+Argument marshalling only: every step of the attention forward runs in the
+library's CUDA kernels. torch supplies device memory and the current
+stream. There is no fallback: if the library is missing or a call fails,
+an exception says so.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_WORKSPACE = 5
+ATTN_F16 = 0
+ATTN_BF16 = 1
+
+# Every symbol include/attn.h declares, with its ctypes signature.
+_VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP]),
+    "attn_fwd_ex": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP, _SZ,
+                         _VP]),
+    "attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_decode_num_splits": (_I, [_I, _I, _I, _I]),
+    "attn_get_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_uint)]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_abi_version": (_I, []),
+    "attn_last_kernel_name": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattn.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with "
+                        "`python -m exact_io_aware_attn_gb300.build` (there is no fallback path)")
+                h = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(h, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = h
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return lib().attn_abi_version()
+
+
+def last_kernel_name() -> str:
+    return lib().attn_last_kernel_name().decode()
+
+
+def workspace_bytes(B, h, T_q, T_kv, d, num_splits=0) -> int:
+    return int(lib().attn_workspace_bytes(B, h, T_q, T_kv, d, num_splits))
+
+
+def decode_num_splits(B, h, T_kv, d) -> int:
+    return int(lib().attn_decode_num_splits(B, h, T_kv, d))
+
+
+def get_device_error(stream=None):
+    """Synchronise the stream, read and clear the device status word.
+    Returns (status, recorded_word)."""
+    word = ctypes.c_uint(0)
+    st = lib().attn_get_device_error(_stream_ptr(stream), ctypes.byref(word))
+    return int(st), int(word.value)
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        if not torch.cuda.is_available():
+            return None
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_q, T_kv, d, scale, causal, dtype,
+            stream_ptr=None, num_splits=None, workspace_ptr=None, workspace_nbytes=0) -> int:
+    """Direct call of attn_fwd (or attn_fwd_ex when num_splits is given) with
+    raw addresses; returns the status code."""
+    L = lib()
+    if num_splits is None:
+        return int(L.attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_q, T_kv, d,
+                              float(scale), int(causal), int(dtype), stream_ptr))
+    return int(L.attn_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_q, T_kv, d,
+                             float(scale), int(causal), int(dtype), int(num_splits),
+                             workspace_ptr, int(workspace_nbytes), stream_ptr))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: q, k, v must be float16 or bfloat16")
+
+
+def attn_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_splits=None,
+             workspace=None, stream=None):
+    """O, lse = softmax(scale * q k^T [+ causal mask]) v, on the GPU.
+
+    q: [B, h, T_q, d]; k, v: [B, h, T_kv, d]; all contiguous CUDA tensors of
+    one 16-bit dtype. Returns (o [B, h, T_q, d] same dtype, lse [B, h, T_q]
+    fp32). `out`/`lse` may be preallocated. With `num_splits` (decode only)
+    the call goes through attn_fwd_ex with a caller workspace (allocated here
+    with torch if not given). Asynchronous on the current (or given) stream.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, h, T, d]")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, h, T_q, d = q.shape
+    T_kv = k.shape[2]
+    if k.shape != (B, h, T_kv, d) or v.shape != (B, h, T_kv, d):
+        raise ValueError("k and v must be [B, h, T_kv, d] with q's B, h and d")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, h, T_q), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse.shape != (B, h, T_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, h, T_q] tensor")
+    sp = _stream_ptr(stream)
+    with torch.cuda.device(q.device):
+        if num_splits is None:
+            st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         B, h, T_q, T_kv, d, scale, causal, dt, sp)
+        else:
+            need = workspace_bytes(B, h, T_q, T_kv, d, num_splits)
+            if workspace is None and need > 0:
+                workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            wp = workspace.data_ptr() if workspace is not None else None
+            wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+            st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         B, h, T_q, T_kv, d, scale, causal, dt, sp, num_splits, wp, wn)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return out, lse

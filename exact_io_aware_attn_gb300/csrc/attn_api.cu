@@ -1,0 +1,252 @@
+// attn_api.cu -- the C ABI of libattn (declared in include/attn.h): argument
+// validation, prefill/decode dispatch, decode split choice, stream-ordered
+// workspace and the device status word. All compute happens in the kernels
+// of prefill_sm103.cu and decode_sm103.cu; nothing here computes attention.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_internal.h"
+#include "attn_status.h"
+
+namespace {
+
+// One status word per device (each device's module instance has its own).
+__device__ unsigned int g_status_word;
+
+unsigned int* status_ptr() {
+  static std::mutex mu;
+  static unsigned int* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int counts[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> g(mu);
+  if (!counts[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+int split_ctas_per_sm(int d, int bf16) {
+  static std::mutex mu;
+  static int cache[64][2][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  std::lock_guard<std::mutex> g(mu);
+  int& c = cache[dev][d == 128][bf16 != 0];
+  if (!c) c = attn::decode_split_ctas_per_sm(d, bf16);
+  return c;
+}
+
+thread_local const char* t_last_kernel = "none";
+
+constexpr int kMaxSplits = 1024;
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na && nb && x < y + nb && y < x + na;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Validates everything that does not depend on the workspace. Sets *empty
+// when the output has no elements (a valid no-op).
+attn_status_t validate(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int h, int T_q, int T_kv, int d, float scale, int causal, int dtype,
+                       bool* empty) {
+  *empty = false;
+  if (B < 0 || h < 0 || T_q < 0 || T_kv < 0) return ATTN_ERR_INVALID_ARG;
+  if (d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * h;
+  if (BH >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (BH == 0 || T_q == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
+  if (T_kv < 1) return ATTN_ERR_INVALID_ARG;
+  if (causal && T_q > T_kv) return ATTN_ERR_INVALID_ARG;
+  if (T_q > 1) {
+    // prefill grid: one CTA per (query tile of 128 rows, b, h)
+    const long long tiles = (static_cast<long long>(T_q) + 127) / 128;
+    if (tiles * BH > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  }
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qo_bytes = static_cast<size_t>(BH) * T_q * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(BH) * T_kv * d * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * T_q * 4;
+  if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, k, kv_bytes) ||
+      overlaps(o, qo_bytes, v, kv_bytes) || overlaps(o, qo_bytes, lse, lse_bytes) ||
+      overlaps(lse, lse_bytes, q, qo_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+      overlaps(lse, lse_bytes, v, kv_bytes))
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// Decode split count chosen by shape: enough partitions that B*h*S CTAs fill
+// the device in whole waves, with at least 64 keys per partition. Among
+// candidates it minimises (waves) x (keys per partition), the critical path
+// of the split kernel, preferring fewer partitions on ties (less merge work).
+int choose_splits(int B, int h, int T_kv, int d, int bf16) {
+  const long long BH = static_cast<long long>(B) * h;
+  const long long cap = static_cast<long long>(sm_count()) * split_ctas_per_sm(d, bf16);
+  const int max_s = static_cast<int>(std::max(1ll, std::min<long long>(kMaxSplits, T_kv / 64)));
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= max_s; ++s) {
+    const long long waves = (BH * s + cap - 1) / cap;
+    const long long keys = (T_kv + s - 1) / s;
+    const long long cost = waves * keys;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+size_t ws_bytes(int B, int h, int d, int splits) {
+  return static_cast<size_t>(B) * h * splits * attn::decode_partial_floats(d) * sizeof(float);
+}
+
+attn_status_t run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                  int T_q, int T_kv, int d, float scale, int causal, int dtype, int num_splits,
+                  void* workspace, size_t workspace_bytes, bool own_workspace, void* stream) {
+  bool empty = false;
+  attn_status_t st = validate(q, k, v, o, lse, B, h, T_q, T_kv, d, scale, causal, dtype, &empty);
+  if (st != ATTN_OK) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  if (empty) {
+    t_last_kernel = "none";
+    return ATTN_OK;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  attn::FwdProblem p{q, k, v, o, lse, B, h, T_q, T_kv, d, scale, causal, dtype == ATTN_BF16 ? 1 : 0,
+                     nullptr};
+  const char* name = "none";
+  if (T_q > 1) {
+    p.status = status_ptr();
+    if (!p.status) return ATTN_ERR_CUDA;
+    if (attn::launch_prefill(p, s, &name) != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_kernel = name;
+    return ATTN_OK;
+  }
+  // the same choice attn_workspace_bytes(..., 0) reports (occupancy of the bf16
+  // and fp16 split kernels is identical)
+  const int splits = num_splits > 0 ? num_splits : choose_splits(B, h, T_kv, d, 1);
+  // split grid: one CTA per (b, h, partition)
+  if (static_cast<long long>(B) * h * splits > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  const size_t need = ws_bytes(B, h, d, splits);
+  if (!own_workspace) {
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ATTN_ERR_WORKSPACE;
+    if (overlaps(workspace, need, q, static_cast<size_t>(B) * h * d * 2) ||
+        overlaps(workspace, need, k, static_cast<size_t>(B) * h * T_kv * d * 2) ||
+        overlaps(workspace, need, v, static_cast<size_t>(B) * h * T_kv * d * 2) ||
+        overlaps(workspace, need, o, static_cast<size_t>(B) * h * d * 2) ||
+        overlaps(workspace, need, lse, static_cast<size_t>(B) * h * 4))
+      return ATTN_ERR_WORKSPACE;
+  }
+  p.status = status_ptr();
+  if (!p.status) return ATTN_ERR_CUDA;
+  float* ws = static_cast<float*>(workspace);
+  if (own_workspace) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), need, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  const cudaError_t e = attn::launch_decode(p, splits, ws, s, &name);
+  if (own_workspace) cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  t_last_kernel = name;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int h, int T_q, int T_kv, int d, float scale, int causal, int dtype,
+                       void* stream) {
+  return run(q, k, v, o, lse, B, h, T_q, T_kv, d, scale, causal, dtype, 0, nullptr, 0, true,
+             stream);
+}
+
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int h, int T_q, int T_kv, int d, float scale, int causal, int dtype,
+                          int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  return run(q, k, v, o, lse, B, h, T_q, T_kv, d, scale, causal, dtype, num_splits, workspace,
+             workspace_bytes, false, stream);
+}
+
+size_t attn_workspace_bytes(int B, int h, int T_q, int T_kv, int d, int num_splits) {
+  if (B < 0 || h < 0 || T_q < 0 || T_kv < 0 || (d != 64 && d != 128)) return 0;
+  if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+  if (T_q != 1 || B == 0 || h == 0 || T_kv < 1) return 0;
+  const int splits = num_splits > 0 ? num_splits : choose_splits(B, h, T_kv, d, 1);
+  return ws_bytes(B, h, d, splits);
+}
+
+int attn_decode_num_splits(int B, int h, int T_kv, int d) {
+  if (B < 1 || h < 1 || T_kv < 1 || (d != 64 && d != 128)) return 0;
+  return choose_splits(B, h, T_kv, d, 1);
+}
+
+attn_status_t attn_get_device_error(void* stream, unsigned int* site) {
+  if (site) *site = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int* p = status_ptr();
+  if (!p) return ATTN_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  if (site) *site = word;
+  if (word == 0) return ATTN_OK;
+  const unsigned int code = word & 0xffu;
+  return code == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+const char* attn_last_kernel_name(void) { return t_last_kernel; }
+
+}  // extern "C"

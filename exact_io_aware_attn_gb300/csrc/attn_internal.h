@@ -1,0 +1,39 @@
+// attn_internal.h -- launchers shared between the C-ABI layer (attn_api.cu)
+// and the kernel translation units. Arguments arrive already validated.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct FwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, h, T_q, T_kv, d;
+  float scale;
+  int causal;
+  int bf16;               // 1 = bf16, 0 = fp16
+  unsigned int* status;   // device status word of the current device
+};
+
+// Prefill (T_q > 1): tcgen05 tensor-core kernel. `name` receives a static
+// kernel name on success.
+cudaError_t launch_prefill(const FwdProblem& p, cudaStream_t stream, const char** name);
+
+// Decode (T_q == 1): split kernel over `num_splits` key partitions writing
+// partials to `ws`, then the merge kernel.
+cudaError_t launch_decode(const FwdProblem& p, int num_splits, float* ws, cudaStream_t stream,
+                          const char** name);
+
+// Split kernel occupancy (CTAs per SM) for the split-count heuristic.
+int decode_split_ctas_per_sm(int d, int bf16);
+
+// Floats per partial: d outputs, then running max and running sum, padded
+// to a 16-byte multiple.
+__host__ __device__ inline constexpr size_t decode_partial_floats(int d) { return static_cast<size_t>(d) + 4; }
+
+}  // namespace attn

@@ -1,0 +1,28 @@
+// attn_status.h -- the device status word shared by all kernels of libattn.
+//
+// Every kernel receives a pointer to one 32-bit word in device memory. A
+// bounded wait that gives up stores (first error wins, atomicCAS from 0):
+//   bits 0-7   status code (ATTN_ERR_TIMEOUT)
+//   bits 8-15  kernel id
+//   bits 16-23 wait site inside that kernel
+// The host reads and clears the word through attn_get_device_error.
+#pragma once
+
+#include <cstdint>
+
+namespace attn {
+
+// Time limit of one device-side wait. Long enough that no healthy wait on
+// a loaded GPU reaches it, short enough that a lost arrival ends the kernel
+// within seconds instead of hanging the device.
+constexpr uint64_t kWaitLimitNs = 2000ull * 1000ull * 1000ull;
+
+constexpr uint32_t kStatusTimeout = 4u;  // == ATTN_ERR_TIMEOUT
+
+enum KernelId : uint32_t { kKernPrefill = 1, kKernDecodeSplit = 2, kKernDecodeCombine = 3, kKernSelftest = 4 };
+
+__host__ __device__ constexpr uint32_t status_word(uint32_t kernel, uint32_t site) {
+  return kStatusTimeout | (kernel << 8) | (site << 16);
+}
+
+}  // namespace attn

@@ -1,0 +1,309 @@
+// decode_sm103.cu -- one query row per (batch, head) against a long KV cache.
+//
+// Decode is a bandwidth-bound streaming reduction over the cached keys and
+// values ("IO-Aware Attention: Tiling the Score Matrix Without
+// Materializing It", section "Where the approach stops helping": with one
+// query row the cost is reading the cache). It is not a dense contraction,
+// so it runs on the CUDA cores with 128-bit coalesced loads, not on tensor
+// cores.
+//
+// To use the whole chip when B*h is small, the keys of each (b, h) are cut
+// into S partitions ("Parallelism and the cost of the split": each of P key
+// partitions produces a partial output and a partial normaliser, combined
+// with the same rescaling by a second kernel):
+//
+//   decode_split_kernel    grid B*h*S: partition s of (b, h) streams its
+//                          keys once, keeps the online-softmax state
+//                          (m, l, o) in fp32 and writes it to the workspace.
+//   decode_combine_kernel  one warp per (b, h): M = max m_s,
+//                          w_s = 2^(m_s - M), L = sum w_s l_s,
+//                          O = sum w_s o_s / L, lse = (M + log2 L) ln 2.
+//
+// Inside a partition, groups of d/8 threads share one key (each thread owns
+// 8 of the d dimensions, one 16-byte load); a warp reads consecutive keys,
+// so every warp-wide load is one contiguous 512-byte segment.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "attn_status.h"
+
+namespace attn {
+
+namespace {
+
+constexpr int kDecThreads = 128;  // 4 warps
+constexpr int kUnroll = 4;        // keys in flight per thread (x2 loads: K and V)
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF16) {
+      // bf16 -> fp32 is a 16-bit shift
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    } else {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 t = __half22float2(h);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+}
+
+// Merge (m2, l2, o2) into (m, l, o); -inf maxima carry weight 0.
+template <int N>
+__device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[N], float m2, float l2,
+                                            const float (&o2)[N]) {
+  const float mn = fmaxf(m, m2);
+  const float ref = (mn == -INFINITY) ? 0.f : mn;
+  const float a = ex2f(m - ref);
+  const float b = ex2f(m2 - ref);
+  l = l * a + l2 * b;
+#pragma unroll
+  for (int i = 0; i < N; ++i) o[i] = o[i] * a + o2[i] * b;
+  m = mn;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,
+                        const uint8_t* __restrict__ v, float* __restrict__ ws, int T_kv, int S,
+                        int chunk, float scale_log2) {
+  constexpr int TPK = D / 8;            // threads per key
+  constexpr int KPW = 32 / TPK;         // keys per warp per load
+  constexpr int SLOTS = (kDecThreads / 32) * KPW;
+  constexpr int ROW = D * 2;            // bytes per key row
+
+  const int s = static_cast<int>(blockIdx.x % static_cast<unsigned>(S));
+  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(S));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % TPK;           // which 8 dims
+  const int slot = warp * KPW + lane / TPK;
+
+  const int lo = s * chunk;
+  const int hi = min(lo + chunk, T_kv);
+
+  float qf[8];
+  unpack8<BF16>(*reinterpret_cast<const uint4*>(q + static_cast<size_t>(bh) * ROW + sub * 16), qf);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
+
+  const uint8_t* kp = k + static_cast<size_t>(bh) * T_kv * ROW + sub * 16;
+  const uint8_t* vp = v + static_cast<size_t>(bh) * T_kv * ROW + sub * 16;
+
+  float m = -INFINITY, l = 0.f;
+  float o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = 0.f;
+
+  for (int base = lo; base < hi; base += SLOTS * kUnroll) {
+    uint4 kr[kUnroll], vr[kUnroll];
+    bool valid[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int key = base + u * SLOTS + slot;
+      valid[u] = key < hi;
+      if (valid[u]) {
+        kr[u] = ld_stream(kp + static_cast<size_t>(key) * ROW);
+        vr[u] = ld_stream(vp + static_cast<size_t>(key) * ROW);
+      } else {
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float sc[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      float kf[8];
+      unpack8<BF16>(kr[u], kf);
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
+#pragma unroll
+      for (int w = 1; w < TPK; w <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
+      sc[u] = valid[u] ? dot : -INFINITY;
+    }
+    float mt = m;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) mt = fmaxf(mt, sc[u]);
+    const float ref = (mt == -INFINITY) ? 0.f : mt;
+    const float a = ex2f(m - ref);
+    l *= a;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] *= a;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const float p = ex2f(sc[u] - ref);
+      l += p;
+      float vf[8];
+      unpack8<BF16>(vr[u], vf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = fmaf(p, vf[i], o[i]);
+    }
+    m = mt;
+  }
+
+  // Merge the key slots of this warp (lanes with the same `sub`).
+#pragma unroll
+  for (int w = TPK; w < 32; w <<= 1) {
+    float o2[8];
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, w);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o2[i] = __shfl_xor_sync(0xffffffffu, o[i], w);
+    merge_state<8>(m, l, o, m2, l2, o2);
+  }
+  // Then the four warps.
+  __shared__ float sh_o[4][D];
+  __shared__ float sh_ml[4][2];
+  if (lane < TPK) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sh_o[warp][sub * 8 + i] = o[i];
+    if (lane == 0) {
+      sh_ml[warp][0] = m;
+      sh_ml[warp][1] = l;
+    }
+  }
+  __syncthreads();
+  if (warp == 0 && lane < TPK) {
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      float o2[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o2[i] = sh_o[w][sub * 8 + i];
+      merge_state<8>(m, l, o, sh_ml[w][0], sh_ml[w][1], o2);
+    }
+    float* part = ws + (static_cast<size_t>(bh) * S + s) * decode_partial_floats(D);
+    *reinterpret_cast<float4*>(part + sub * 8) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4*>(part + sub * 8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    if (lane == 0) *reinterpret_cast<float4*>(part + D) = make_float4(m, l, 0.f, 0.f);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128)
+    decode_combine_kernel(const float* __restrict__ ws, uint8_t* __restrict__ out,
+                          float* __restrict__ lse, int BH, int S) {
+  constexpr int PER = D / 32;   // dims per lane
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x * 4 + warp;
+  if (bh >= BH) return;
+  const size_t stride = decode_partial_floats(D);
+  const float* part = ws + static_cast<size_t>(bh) * S * stride;
+
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, part[s * stride + D]);
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
+  // every row has at least one key, so M is finite
+  float L = 0.f;
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float* ps = part + s * stride;
+    const float ms = ps[D];
+    const float w = (ms == -INFINITY) ? 0.f : ex2f(ms - M);
+    L = fmaf(w, ps[D + 1], L);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, ps[lane * PER + i], acc[i]);
+  }
+  const float inv = 1.f / L;
+  uint8_t* orow = out + static_cast<size_t>(bh) * D * 2 + lane * PER * 2;
+  if constexpr (PER == 2) {
+    uint32_t w;
+    if constexpr (BF16) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+      w = *reinterpret_cast<uint32_t*>(&h);
+    } else {
+      __half2 h = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
+      w = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint32_t*>(orow) = w;
+  } else {
+    uint32_t w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if constexpr (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+      } else {
+        __half2 h = __floats2half2_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+      }
+    }
+    *reinterpret_cast<uint2*>(orow) = make_uint2(w[0], w[1]);
+  }
+  if (lane == 0) lse[bh] = (M + __log2f(L)) * 0.69314718055994531f;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_t(const FwdProblem& p, int S, float* ws, cudaStream_t stream) {
+  const int BH = p.B * p.h;
+  const int chunk = (p.T_kv + S - 1) / S;
+  const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+  dim3 g1(static_cast<unsigned>(S) * static_cast<unsigned>(BH));
+  decode_split_kernel<D, BF16><<<g1, kDecThreads, 0, stream>>>(
+      static_cast<const uint8_t*>(p.q), static_cast<const uint8_t*>(p.k),
+      static_cast<const uint8_t*>(p.v), ws, p.T_kv, S, chunk, scale_log2);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2(static_cast<unsigned>((BH + 3) / 4));
+  decode_combine_kernel<D, BF16><<<g2, 128, 0, stream>>>(ws, static_cast<uint8_t*>(p.o), p.lse, BH, S);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const FwdProblem& p, int num_splits, float* ws, cudaStream_t stream,
+                          const char** name) {
+  cudaError_t e;
+  if (p.d == 64) {
+    e = p.bf16 ? launch_t<64, true>(p, num_splits, ws, stream)
+               : launch_t<64, false>(p, num_splits, ws, stream);
+    *name = p.bf16 ? "decode_split_d64_bf16+decode_combine" : "decode_split_d64_f16+decode_combine";
+  } else {
+    e = p.bf16 ? launch_t<128, true>(p, num_splits, ws, stream)
+               : launch_t<128, false>(p, num_splits, ws, stream);
+    *name = p.bf16 ? "decode_split_d128_bf16+decode_combine" : "decode_split_d128_f16+decode_combine";
+  }
+  return e;
+}
+
+int decode_split_ctas_per_sm(int d, int bf16) {
+  int n = 0;
+  cudaError_t e;
+  if (d == 64)
+    e = bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<64, true>, kDecThreads, 0)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<64, false>, kDecThreads, 0);
+  else
+    e = bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<128, true>, kDecThreads, 0)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<128, false>, kDecThreads, 0);
+  return (e == cudaSuccess && n > 0) ? n : 8;
+}
+
+}  // namespace attn

@@ -1,0 +1,155 @@
+/*
+ * attn.h -- C ABI of libattn: exact IO-aware attention forward on GB300.
+ *
+ * What it computes (per batch element b and head h):
+ *
+ *     S = scale * Q K^T            (T_q x T_kv, never written to memory)
+ *     P = softmax(S) row by row    (T_q x T_kv, never written to memory)
+ *     O = P V                      (T_q x d)
+ *     lse[i] = ln sum_j exp(S[i][j])
+ *
+ * following "FlashAttention IO-aware tiling lab" (the definition
+ * S = QK^T/sqrt(d), P = softmax(S), O = PV and the kernel phases) and
+ * "IO-Aware Attention: Tiling the Score Matrix Without Materializing It",
+ * section "Softmax over blocks, exactly" (running maximum m, running sum l,
+ * rescaled accumulator o, result o/l). The problem statement -- Q is T_q x d,
+ * K and V are T_kv x d per head, over B sequences and h heads, with an
+ * optional causal mask -- is that of "Attention and Its Computational Cost",
+ * section "What is being computed". lse is the per-row normalisation
+ * constant kept for a backward pass ("IO-Aware Attention ...", section
+ * "What has to stay in fast memory").
+ *
+ * Causal mask: key j is visible to query row i iff j <= i + (T_kv - T_q)
+ * (bottom-right alignment; for T_q == T_kv row i sees keys 0..i, and a single
+ * query sees the whole cache). A masked row never has zero visible keys
+ * because T_q <= T_kv is required.
+ *
+ * Dispatch: T_q == 1 runs the split-KV decode path (a split kernel over key
+ * partitions, then an exact merge kernel: "IO-Aware Attention ...", section
+ * "Parallelism and the cost of the split"); T_q > 1 runs the tensor-core
+ * prefill kernel.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major, contiguous [B][h][T][d] in device memory,
+ *     all four of q, k, v, o in the same 16-bit type (dtype), each base
+ *     16-byte aligned. lse is fp32 [B][h][T_q], 4-byte aligned.
+ *   - The caller owns every buffer; the library keeps no pointer after the
+ *     work it enqueued has finished. o and lse must not overlap q, k or v
+ *     or each other.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Calls are asynchronous: ATTN_OK means "validated and
+ *     enqueued". Arguments are checked before anything is enqueued; an
+ *     invalid call enqueues nothing and touches no buffer.
+ *   - Supported set: d in {64, 128}; dtype ATTN_F16 or ATTN_BF16;
+ *     scale finite and > 0; B, h, T_q >= 0 (a zero makes the call an empty
+ *     no-op returning ATTN_OK); T_kv >= 1 whenever the output is non-empty;
+ *     causal requires T_q <= T_kv; B*h < 2^31 and T_q, T_kv < 2^31.
+ *   - Accumulation and rescaling are fp32; O is rounded once to the 16-bit
+ *     type (round to nearest even).
+ *   - Errors are return codes; nothing aborts or prints. A device-side wait
+ *     that exceeds its time limit does not hang: the kernel records
+ *     ATTN_ERR_TIMEOUT in a device status word, leaves its outputs undefined
+ *     and returns; read it with attn_get_device_error.
+ */
+#ifndef EXACT_IO_AWARE_ATTN_H
+#define EXACT_IO_AWARE_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size, bad scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request outside the supported set (e.g. d = 96) */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+  ATTN_ERR_TIMEOUT = 4,     /* a device-side bounded wait gave up (see attn_get_device_error) */
+  ATTN_ERR_WORKSPACE = 5    /* workspace missing, too small or misaligned */
+} attn_status_t;
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/*
+ * attn_fwd -- the whole forward: O and lse from Q, K, V.
+ *   q     [B][h][T_q][d]   16-bit, read only
+ *   k, v  [B][h][T_kv][d]  16-bit, read only
+ *   o     [B][h][T_q][d]   16-bit, written
+ *   lse   [B][h][T_q]      fp32, written (natural log, scaled-score units)
+ *   scale multiplies Q K^T (1/sqrt(d) for standard attention)
+ *   causal 0 or 1
+ * The decode path (T_q == 1) needs a workspace of attn_workspace_bytes(...,
+ * 0) bytes; attn_fwd takes it from the stream-ordered allocator
+ * (cudaMallocAsync/cudaFreeAsync on `stream`, no host synchronisation). The
+ * prefill path needs no workspace.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int h, int T_q, int T_kv, int d, float scale, int causal,
+                       int dtype, void* stream);
+
+/*
+ * attn_fwd_ex -- attn_fwd with caller-chosen decode split count and
+ * caller-owned workspace.
+ *   num_splits  key partitions per (b, h) for the decode path: 0 = the
+ *               library's choice by shape, else 1..1024 (a partition that
+ *               gets no key contributes weight 0). Ignored for T_q > 1.
+ *   workspace   device memory, 16-byte aligned, at least
+ *               attn_workspace_bytes(B, h, T_q, T_kv, d, num_splits) bytes;
+ *               may be NULL when that size is 0. Contents on entry are
+ *               ignored; it must stay allocated until the work completes.
+ * Returns ATTN_ERR_WORKSPACE if the workspace is needed and missing, too
+ * small or misaligned.
+ */
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int h, int T_q, int T_kv, int d, float scale, int causal,
+                          int dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
+ * attn_workspace_bytes -- bytes of workspace attn_fwd_ex needs for this
+ * shape (0 for the prefill path). num_splits as in attn_fwd_ex (0 = the
+ * library's choice). Returns 0 for invalid sizes. The decode workspace holds
+ * one partial (running max, running sum, unnormalised output of d floats)
+ * per (b, h, split): B*h*S*(d+4)*4 bytes.
+ */
+size_t attn_workspace_bytes(int B, int h, int T_q, int T_kv, int d, int num_splits);
+
+/*
+ * attn_decode_num_splits -- the split count the library chooses for a
+ * decode call of this shape on the current device (0 if the shape is
+ * invalid). Deterministic for a given device.
+ */
+int attn_decode_num_splits(int B, int h, int T_kv, int d);
+
+/*
+ * attn_get_device_error -- synchronises `stream`, then reads and clears the
+ * current device's status word. Returns ATTN_OK if no kernel recorded an
+ * error since the last read, ATTN_ERR_TIMEOUT if a bounded wait gave up, or
+ * ATTN_ERR_CUDA if the synchronisation itself failed. If `site` is not NULL
+ * it receives the recorded word (0 if none): bits 0-7 the status code,
+ * bits 8-15 the kernel, bits 16-23 the wait site.
+ */
+attn_status_t attn_get_device_error(void* stream, unsigned int* site);
+
+/* attn_status_string -- static, NUL-terminated name of a status code. */
+const char* attn_status_string(int status);
+
+/* attn_abi_version -- ATTN_ABI_VERSION of the library actually loaded. */
+int attn_abi_version(void);
+
+/*
+ * attn_last_kernel_name -- static name of the kernel family the last
+ * successful attn_fwd/attn_fwd_ex call on this host thread enqueued
+ * ("prefill_tcgen05_d64_bf16", "decode_split_d64_bf16+decode_combine", ...
+ * or "none" for an empty call), so a benchmark can record which kernel ran.
+ */
+const char* attn_last_kernel_name(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_IO_AWARE_ATTN_H */

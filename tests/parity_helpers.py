@@ -1,0 +1,80 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C
+ABI, run the oracle on the very same 16-bit inputs, compare."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from exact_io_aware_attn_gb300 import _lib
+from exact_io_aware_attn_gb300.inputs import BF16, F16, make_qkv
+
+# Tolerances the method states for 16-bit inputs with fp32 accumulation.
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+# A tighter, dtype-aware element-wise gate: P and O are each rounded once to
+# the 16-bit type (relative 2^-9 for bf16, 2^-11 for fp16), so a correct
+# kernel stays within about twice the output rounding plus a small absolute
+# term; systematic mistakes (a wrong mask element, a missed rescale) do not.
+TIGHT = {BF16: (2.0 ** -8, 8e-3), F16: (2.0 ** -10, 2e-3)}
+
+
+def oracle_scale(scale: float) -> float:
+    """The float32 value the kernel receives, as float64."""
+    return float(np.float32(scale))
+
+
+def gpu_fwd(q, k, v, causal, scale=None, num_splits=None, check_status=True):
+    """q, k, v: CPU 16-bit tensors. Returns (o float64 [B,h,T_q,d], lse float64)."""
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.full_like(qd, float("nan"))              # unwritten elements show up
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=dev)
+    _lib.attn_fwd(qd, kd, vd, scale=scale, causal=causal, out=o, lse=lse, num_splits=num_splits)
+    torch.cuda.synchronize()
+    if check_status:
+        st, word = _lib.get_device_error()
+        assert st == _lib.ATTN_OK, f"device status {st} word {word:#x}"
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def oracle_fwd(q, k, v, causal, scale=None, rows=None):
+    d = q.shape[-1]
+    s = oracle_scale(d ** -0.5 if scale is None else scale)
+    return oracle.standard_attention(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                     scale=s, causal=causal, rows=rows)
+
+
+def compare(o, lse, o_ref, lse_ref, dtype, what=""):
+    assert np.isfinite(o).all(), f"{what}: non-finite output (unwritten or NaN)"
+    assert np.isfinite(lse).all(), f"{what}: non-finite lse"
+    err_o = np.abs(o - o_ref)
+    err_l = np.abs(lse - lse_ref)
+    assert err_o.max() <= O_TOL, f"{what}: max|dO| = {err_o.max():.3e} > {O_TOL}"
+    assert err_l.max() <= LSE_TOL, f"{what}: max|dlse| = {err_l.max():.3e} > {LSE_TOL}"
+    rel, ab = TIGHT[dtype]
+    bound = rel * np.abs(o_ref) + ab
+    worst = np.argmax(err_o - bound)
+    assert (err_o <= bound).all(), (
+        f"{what}: element {np.unravel_index(worst, o.shape)} off by "
+        f"{err_o.flat[worst]:.3e} (bound {bound.flat[worst]:.3e})")
+    return float(err_o.max()), float(err_l.max()), float(np.sqrt((err_o ** 2).mean()))
+
+
+def check_case(B, h, T_q, T_kv, d, dtype, causal, mult=1.0, seed=0, scale=None, num_splits=None):
+    q, k, v = make_qkv(B, h, T_q, T_kv, d, dtype, mult, seed)
+    o, lse = gpu_fwd(q, k, v, causal, scale, num_splits)
+    o_ref, lse_ref = oracle_fwd(q, k, v, causal, scale)
+    return compare(o, lse, o_ref, lse_ref, dtype,
+                   f"B{B} h{h} Tq{T_q} Tkv{T_kv} d{d} {'bf16' if dtype else 'f16'} causal={causal}")
+
+
+def sample_rows(T_q, n_random=12, seed=0):
+    """Rows that exercise every kind of tile position: first/last rows of
+    tiles, the ragged tail, and a few random ones."""
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 63, 64, 127, 128, 129, 255, 256, T_q // 2, T_q - 129, T_q - 128, T_q - 2, T_q - 1]
+    rows = [r for r in fixed if 0 <= r < T_q]
+    rows += list(rng.integers(0, T_q, size=n_random))
+    return np.unique(np.array(rows, dtype=np.int64))

@@ -1,0 +1,176 @@
+"""The C-ABI library on any host (no GPU needed, no compute call made).
+
+Checks that libattn.so builds, loads and exports every symbol include/attn.h
+declares, and that every invalid argument is rejected with the right status
+before anything is enqueued (validation runs before the first CUDA call, so
+these calls are safe without a GPU).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_attn_gb300 import _lib, build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("attn_fwd", "attn_fwd_ex", "attn_workspace_bytes", "attn_get_device_error",
+                 "attn_status_string", "attn_abi_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"libattn.so does not export {name}"
+        assert name in _lib.SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_binding_declares_nothing_extra():
+    assert sorted(_lib.SIGNATURES) == declared_functions()
+
+
+def test_abi_version_matches_header(L):
+    m = re.search(r"#define ATTN_ABI_VERSION (\d+)", open(HEADER).read())
+    assert L.attn_abi_version() == int(m.group(1))
+
+
+def test_status_strings(L):
+    for code, name in enumerate(["ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
+                                 "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE"]):
+        assert _lib.status_string(code) == name
+    assert _lib.status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+# fake, 16-byte aligned, non-overlapping addresses: validation never
+# dereferences them
+Q, K, V, O, LSE, WS = (0x100000 * i for i in range(1, 7))
+GOOD = dict(B=2, h=3, T_q=100, T_kv=200, d=64, scale=0.125, causal=1, dtype=_lib.ATTN_BF16)
+
+
+def call(**over):
+    a = dict(GOOD)
+    ptrs = dict(q=Q, k=K, v=V, o=O, lse=LSE)
+    for key in list(over):
+        if key in ptrs:
+            ptrs[key] = over.pop(key)
+    a.update(over)
+    return _lib.fwd_raw(ptrs["q"], ptrs["k"], ptrs["v"], ptrs["o"], ptrs["lse"], a["B"], a["h"],
+                        a["T_q"], a["T_kv"], a["d"], a["scale"], a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(k=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(v=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(o=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(h=-2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(T_q=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(T_kv=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(T_kv=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=-64), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(d=32), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(T_q=300, T_kv=200), _lib.ATTN_ERR_INVALID_ARG),      # causal needs T_q <= T_kv
+    (dict(q=Q + 8), _lib.ATTN_ERR_INVALID_ARG),                 # misaligned
+    (dict(k=K + 2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(o=O + 4), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(lse=LSE + 2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-0.125), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(o=Q), _lib.ATTN_ERR_INVALID_ARG),                     # output aliases an input
+    (dict(o=K + 64), _lib.ATTN_ERR_INVALID_ARG),                # overlapping ranges
+    (dict(lse=V), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(lse=O + 16), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(B=1 << 16, h=1 << 15), _lib.ATTN_ERR_UNSUPPORTED),    # B*h >= 2^31
+])
+def test_invalid_arguments_rejected_before_launch(L, over, status):
+    assert call(**over) == status
+
+
+@pytest.mark.parametrize("over", [dict(B=0), dict(h=0), dict(T_q=0),
+                                  dict(B=0, q=0, k=0, v=0, o=0, lse=0),
+                                  dict(T_q=0, T_kv=0, causal=0)])
+def test_empty_problem_is_a_no_op(L, over):
+    assert call(**over) == _lib.ATTN_OK
+    assert _lib.last_kernel_name() == "none"
+
+
+def _ex(num_splits, ws, nbytes, **over):
+    a = dict(GOOD, T_q=1, causal=0)
+    a.update(over)
+    return _lib.fwd_raw(Q, K, V, O, LSE, a["B"], a["h"], a["T_q"], a["T_kv"], a["d"], a["scale"],
+                        a["causal"], a["dtype"], None, num_splits, ws, nbytes)
+
+
+def test_workspace_bytes_formula(L):
+    B, h, T_kv = 32, 12, 16384
+    for d in (64, 128):
+        for s in (1, 16, 19, 64, 1024):
+            assert _lib.workspace_bytes(B, h, 1, T_kv, d, s) == B * h * s * (d + 4) * 4
+    # prefill needs no workspace; invalid sizes report 0
+    assert _lib.workspace_bytes(B, h, 1024, 1024, 64, 0) == 0
+    assert _lib.workspace_bytes(B, h, 1, T_kv, 96, 16) == 0
+    assert _lib.workspace_bytes(B, h, 1, T_kv, 64, 1025) == 0
+    assert _lib.workspace_bytes(-1, h, 1, T_kv, 64, 16) == 0
+
+
+def test_auto_split_count_is_in_range(L):
+    for (B, h, T) in ((32, 12, 16384), (1, 12, 16384), (1, 1, 100), (64, 12, 1024), (1, 1, 1)):
+        s = _lib.decode_num_splits(B, h, T, 64)
+        assert 1 <= s <= 1024
+        assert s == 1 or -(-T // s) >= 64       # at least 64 keys per partition
+        assert _lib.workspace_bytes(B, h, 1, T, 64, 0) == B * h * s * 68 * 4
+    assert _lib.decode_num_splits(0, 12, 100, 64) == 0
+
+
+@pytest.mark.parametrize("num_splits,ws,nbytes,status", [
+    (-1, WS, 1 << 20, _lib.ATTN_ERR_INVALID_ARG),
+    (1025, WS, 1 << 20, _lib.ATTN_ERR_INVALID_ARG),
+    (16, 0, 1 << 20, _lib.ATTN_ERR_WORKSPACE),            # missing
+    (16, WS, 100, _lib.ATTN_ERR_WORKSPACE),               # too small
+    (16, WS + 4, 1 << 20, _lib.ATTN_ERR_WORKSPACE),       # misaligned
+    (16, K, 1 << 20, _lib.ATTN_ERR_WORKSPACE),            # overlaps an input
+])
+def test_decode_workspace_errors(L, num_splits, ws, nbytes, status):
+    assert _ex(num_splits, ws, nbytes) == status
+
+
+def test_python_binding_rejects_cpu_tensors(L):
+    import torch
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        _lib.attn_fwd(x, x, x)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libattn.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.lib()
