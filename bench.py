@@ -408,6 +408,41 @@ def run_ours(args):
     return 0
 
 
+def run_kernel_case(args):
+    """Profiling mode: one call of the step (--kernel-case prefill|decode),
+    repeated --steps times after --warmup calls; prints a one-line summary,
+    no benchmark JSON. --case-batch shrinks B for small ncu captures."""
+    import dataclasses
+
+    import torch
+
+    from exact_io_aware_attn_gb300 import _lib, build as build_mod
+    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL, make_workload
+
+    build_mod.build()
+    w = GPT2_PREFILL if args.kernel_case == "prefill" else DECODE
+    if args.case_batch:
+        w = dataclasses.replace(w, B=args.case_batch)
+    q, k, v = (t.cuda() for t in make_workload(w))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    for _ in range(args.warmup):
+        _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+    b.record()
+    torch.cuda.synchronize()
+    st, word = _lib.get_device_error()
+    if st != _lib.ATTN_OK:
+        raise SystemExit(f"device status {st} ({word:#x})")
+    print(f"{args.kernel_case} {w.name} B={w.B}: {_lib.last_kernel_name()} "
+          f"{a.elapsed_time(b) / max(1, args.steps) * 1e3:.1f} us/call", flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[1])
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,7 +450,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-case", choices=["prefill", "decode"],
+                    help="profiling mode: run only this call of the step")
+    ap.add_argument("--case-batch", type=int, default=None,
+                    help="batch size override for --kernel-case")
     args = ap.parse_args(argv)
+    if args.kernel_case:
+        return run_kernel_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

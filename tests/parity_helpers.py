@@ -10,14 +10,17 @@ import oracle
 from exact_io_aware_attn_gb300 import _lib
 from exact_io_aware_attn_gb300.inputs import BF16, F16, make_qkv
 
-# Tolerances the method states for 16-bit inputs with fp32 accumulation.
+# Tolerances the method states for 16-bit inputs with fp32 accumulation
+# (N(0,1) workloads, |O| of order one).
 O_TOL = 2e-2
 LSE_TOL = 1e-3
-# A tighter, dtype-aware element-wise gate: P and O are each rounded once to
-# the 16-bit type (relative 2^-9 for bf16, 2^-11 for fp16), so a correct
-# kernel stays within about twice the output rounding plus a small absolute
-# term; systematic mistakes (a wrong mask element, a missed rescale) do not.
-TIGHT = {BF16: (2.0 ** -8, 8e-3), F16: (2.0 ** -10, 2e-3)}
+# Element-wise gate derived from the arithmetic: P is rounded once to the
+# 16-bit type before the PV product and O is rounded once at the end, each
+# with unit roundoff u (2^-8 bf16, 2^-11 fp16); accumulation is fp32. The
+# first rounding moves O_i by at most u * sum_j p_ij |v_jd| / l_i -- the
+# attention-weighted mean of |V|, which the oracle computes by running on
+# |V| -- and the second by u * |O_i|. The gate allows 1.25x that plus 1e-4.
+UNIT_ROUNDOFF = {BF16: 2.0 ** -8, F16: 2.0 ** -11}
 
 
 def oracle_scale(scale: float) -> float:
@@ -40,22 +43,31 @@ def gpu_fwd(q, k, v, causal, scale=None, num_splits=None, check_status=True):
 
 
 def oracle_fwd(q, k, v, causal, scale=None, rows=None):
+    """(O, lse, O_abs): the oracle on (q, k, v), and O_abs = the oracle's
+    output for |v| (the same weights applied to |V|)."""
     d = q.shape[-1]
     s = oracle_scale(d ** -0.5 if scale is None else scale)
-    return oracle.standard_attention(q.double().numpy(), k.double().numpy(), v.double().numpy(),
-                                     scale=s, causal=causal, rows=rows)
+    qn, kn, vn = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    o_ref, lse_ref = oracle.standard_attention(qn, kn, vn, scale=s, causal=causal, rows=rows)
+    o_abs, _ = oracle.standard_attention(qn, kn, np.abs(vn), scale=s, causal=causal, rows=rows)
+    return o_ref, lse_ref, o_abs
 
 
-def compare(o, lse, o_ref, lse_ref, dtype, what=""):
+def compare(o, lse, ref, dtype, what="", absolute=True):
+    """absolute=True also applies the fixed tolerances stated for the N(0,1)
+    workloads; inputs scaled far beyond that (|O| up to ~12) are held to the
+    rounding-derived gate alone."""
+    o_ref, lse_ref, o_abs = ref
     assert np.isfinite(o).all(), f"{what}: non-finite output (unwritten or NaN)"
     assert np.isfinite(lse).all(), f"{what}: non-finite lse"
     err_o = np.abs(o - o_ref)
     err_l = np.abs(lse - lse_ref)
-    assert err_o.max() <= O_TOL, f"{what}: max|dO| = {err_o.max():.3e} > {O_TOL}"
+    if absolute:
+        assert err_o.max() <= O_TOL, f"{what}: max|dO| = {err_o.max():.3e} > {O_TOL}"
     assert err_l.max() <= LSE_TOL, f"{what}: max|dlse| = {err_l.max():.3e} > {LSE_TOL}"
-    rel, ab = TIGHT[dtype]
-    bound = rel * np.abs(o_ref) + ab
-    worst = np.argmax(err_o - bound)
+    u = UNIT_ROUNDOFF[dtype]
+    bound = 1.25 * u * (o_abs + np.abs(o_ref)) + 1e-4
+    worst = np.argmax(err_o / bound)
     assert (err_o <= bound).all(), (
         f"{what}: element {np.unravel_index(worst, o.shape)} off by "
         f"{err_o.flat[worst]:.3e} (bound {bound.flat[worst]:.3e})")
@@ -65,9 +77,10 @@ def compare(o, lse, o_ref, lse_ref, dtype, what=""):
 def check_case(B, h, T_q, T_kv, d, dtype, causal, mult=1.0, seed=0, scale=None, num_splits=None):
     q, k, v = make_qkv(B, h, T_q, T_kv, d, dtype, mult, seed)
     o, lse = gpu_fwd(q, k, v, causal, scale, num_splits)
-    o_ref, lse_ref = oracle_fwd(q, k, v, causal, scale)
-    return compare(o, lse, o_ref, lse_ref, dtype,
-                   f"B{B} h{h} Tq{T_q} Tkv{T_kv} d{d} {'bf16' if dtype else 'f16'} causal={causal}")
+    ref = oracle_fwd(q, k, v, causal, scale)
+    return compare(o, lse, ref, dtype,
+                   f"B{B} h{h} Tq{T_q} Tkv{T_kv} d{d} {'bf16' if dtype else 'f16'} causal={causal}",
+                   absolute=mult <= 1.0)
 
 
 def sample_rows(T_q, n_random=12, seed=0):
