@@ -36,7 +36,11 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_abi_version": (_I, []),
     "attn_last_kernel_name": (ctypes.c_char_p, []),
+    "attn_fwd_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP]),
 }
+
+# Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -117,6 +121,43 @@ def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_q, T_kv, d, scale, caus
     return int(L.attn_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_q, T_kv, d,
                              float(scale), int(causal), int(dtype), int(num_splits),
                              workspace_ptr, int(workspace_nbytes), stream_ptr))
+
+
+def fwd_decode_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_kv, d, scale, dtype,
+                           num_splits=0, stream_ptr=None) -> int:
+    """Direct call of attn_fwd_decode_noalloc; returns the status code."""
+    return int(lib().attn_fwd_decode_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_kv, d,
+                                             float(scale), int(dtype), int(num_splits),
+                                             stream_ptr))
+
+
+def attn_fwd_decode_noalloc(q, k, v, *, out, lse, scale=None, num_splits=0, stream=None):
+    """Decode (one query row per (b, h)) into caller-provided `out` and `lse`
+    without allocating anything: for callers that cannot allocate device
+    memory at call time. The partials live in a fixed library-owned device
+    array (NOALLOC_SCRATCH_BYTES per device); calls that overlap on the GPU
+    race on it. q: [B, h, 1, d]; k, v: [B, h, T_kv, d]; out like q; lse
+    [B, h, 1] fp32."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    B, h, T_q, d = q.shape
+    if T_q != 1:
+        raise ValueError("attn_fwd_decode_noalloc takes one query row per (b, h)")
+    T_kv = k.shape[2]
+    if k.shape != (B, h, T_kv, d) or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if not (q.dtype == k.dtype == v.dtype == out.dtype) or lse.dtype != torch.float32:
+        raise TypeError("q, k, v, out share one 16-bit dtype; lse is fp32")
+    if scale is None:
+        scale = d ** -0.5
+    st = fwd_decode_noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, h, T_kv, d, scale, _dtype_code(q), num_splits,
+                                _stream_ptr(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_decode_noalloc")
+    return out, lse
 
 
 def _dtype_code(t):

@@ -25,7 +25,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 
-SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu"]
+SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "attn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

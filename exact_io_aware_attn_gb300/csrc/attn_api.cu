@@ -69,6 +69,11 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+}  // namespace
+
+namespace attn {
+namespace detail {
+
 // Validates everything that does not depend on the workspace. Sets *empty
 // when the output has no elements (a valid no-op).
 attn_status_t validate(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -129,6 +134,14 @@ int choose_splits(int B, int h, int T_kv, int d, int bf16) {
   }
   return best;
 }
+
+}  // namespace detail
+}  // namespace attn
+
+namespace {
+
+using attn::detail::choose_splits;
+using attn::detail::validate;
 
 size_t ws_bytes(int B, int h, int d, int splits) {
   return static_cast<size_t>(B) * h * splits * attn::decode_partial_floats(d) * sizeof(float);

@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cuda_runtime.h>
 
+#include "attn.h"
+
 namespace attn {
 
 struct FwdProblem {
@@ -31,6 +33,15 @@ cudaError_t launch_decode(const FwdProblem& p, int num_splits, float* ws, cudaSt
 
 // Split kernel occupancy (CTAs per SM) for the split-count heuristic.
 int decode_split_ctas_per_sm(int d, int bf16);
+
+namespace detail {
+// Argument checks shared by every entry point (attn_api.cu); *empty is set
+// when the output has no elements.
+attn_status_t validate(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+             int T_q, int T_kv, int d, float scale, int causal, int dtype, bool* empty);
+// Decode split count chosen by shape on the current device (attn_api.cu).
+int choose_splits(int B, int h, int T_kv, int d, int bf16);
+}  // namespace detail
 
 // Floats per partial: d outputs, then running max and running sum, padded
 // to a 16-byte multiple.

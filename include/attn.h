@@ -148,6 +148,33 @@ int attn_abi_version(void);
  */
 const char* attn_last_kernel_name(void);
 
+/*
+ * attn_fwd_decode_noalloc -- the decode path (T_q == 1) without any
+ * allocation, for callers that cannot allocate device memory at call time
+ * (their memory is owned by another allocator, such as a serving engine that
+ * reserves all of HBM up front, or they cannot accept the synchronisation a
+ * cudaMalloc/cudaFree may bring). The pages have no counterpart: this is a
+ * deployment variant of attn_fwd for one query row per (b, h).
+ *
+ * Same arguments and layout as attn_fwd with T_q = 1 (q, o: [B][h][1][d],
+ * k, v: [B][h][T_kv][d]; a single query sees every key, so there is no
+ * causal flag), plus num_splits as in attn_fwd_ex (0 = the library's
+ * choice). It makes no cudaMalloc/cudaFree or other allocating call: the
+ * split partials (B*h*S*(d+4)*4 bytes) live in a fixed device array owned by
+ * the library, ATTN_NOALLOC_SCRATCH_BYTES on every device that loads it,
+ * held until the library is unloaded. A shape whose partials do not fit
+ * returns ATTN_ERR_WORKSPACE before anything is enqueued (fewer splits may
+ * fit). The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls on a device share the array: calls whose kernels overlap on the
+ * GPU (e.g. on two streams without ordering) race and give wrong results.
+ * The array keeps the last call's partials; nothing in it needs clearing.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+attn_status_t attn_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o,
+                                      float* lse, int B, int h, int T_kv, int d, float scale,
+                                      int dtype, int num_splits, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
