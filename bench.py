@@ -416,18 +416,21 @@ def run_ours(args):
 
 
 def run_kernel_case(args):
-    """Profiling mode: one call of the step (--kernel-case prefill|decode),
-    repeated --steps times after --warmup calls; prints a one-line summary,
-    no benchmark JSON. --case-batch shrinks B for small ncu captures."""
+    """Profiling mode: one call of the step (--kernel-case prefill|decode), or
+    any named workload (--kernel-case NAME, see inputs.WORKLOADS), repeated
+    --steps times after --warmup calls; prints one JSON line with the mean
+    time per call and its throughput, no benchmark line. --case-batch
+    overrides B for small ncu captures."""
     import dataclasses
 
     import torch
 
-    from exact_io_aware_attn_gb300 import _lib, build as build_mod
-    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL, make_workload
+    from exact_io_aware_attn_gb300 import _lib, build as build_mod, cost
+    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL, WORKLOADS, make_workload
 
     build_mod.build()
-    w = GPT2_PREFILL if args.kernel_case == "prefill" else DECODE
+    named = {w.name: w for w in WORKLOADS}
+    w = {"prefill": GPT2_PREFILL, "decode": DECODE}.get(args.kernel_case) or named[args.kernel_case]
     if args.case_batch:
         w = dataclasses.replace(w, B=args.case_batch)
     q, k, v = (t.cuda() for t in make_workload(w))
@@ -445,8 +448,15 @@ def run_kernel_case(args):
     st, word = _lib.get_device_error()
     if st != _lib.ATTN_OK:
         raise SystemExit(f"device status {st} ({word:#x})")
-    print(f"{args.kernel_case} {w.name} B={w.B}: {_lib.last_kernel_name()} "
-          f"{a.elapsed_time(b) / max(1, args.steps) * 1e3:.1f} us/call", flush=True)
+    sec = a.elapsed_time(b) / max(1, args.steps) * 1e-3
+    fl = cost.flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
+    by = cost.min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d)
+    peaks = load_peaks()
+    print(json.dumps({"workload": w.name, "B": w.B, "kernel": _lib.last_kernel_name(),
+                      "us_per_call": sec * 1e6, "tflops": fl / sec / 1e12,
+                      "gbs": by / sec / 1e9,
+                      "frac_tensor_peak": fl / sec / 1e12 / peaks["bf16_tflops"],
+                      "frac_hbm_peak": by / sec / 1e9 / peaks["hbm_gbs"]}), flush=True)
     return 0
 
 
@@ -457,8 +467,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", choices=["prefill", "decode"],
-                    help="profiling mode: run only this call of the step")
+    ap.add_argument("--kernel-case", metavar="prefill|decode|WORKLOAD",
+                    help="profiling mode: run only this call of the step, or a named workload")
     ap.add_argument("--case-batch", type=int, default=None,
                     help="batch size override for --kernel-case")
     args = ap.parse_args(argv)

@@ -1,37 +1,45 @@
 // prefill_sm103.cu -- exact attention forward for T_q > 1 on GB300 tensor cores.
 //
-// One CTA owns one tile of 128 query rows of one (batch, head) and walks the
-// key/value tiles of 128 keys that the tile can see:
+// A persistent CTA owns a sequence of work units; a unit is a pair of
+// 128-row query tiles (A and B) of one (batch, head) that share one stream of
+// 128-key K/V tiles. Roles (384 threads, three warpgroups):
 //
-//   warp 0        TMA producer: Q tile once, then K_j and V_j tiles into a
-//                 multi-stage shared-memory ring (128-byte swizzle).
-//   warp 1        TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into a
-//                 double-buffered TMEM score tile; O += P_j V_j into the TMEM
-//                 output accumulator (fp32).
-//   warps 2..5    softmax: thread t owns query row t (TMEM lane t). It reads
-//                 its score row from TMEM, applies the causal/tail mask,
-//                 updates the running max m and running sum l, writes
-//                 P_j = exp(scale*S_j - m) as 16-bit into shared memory for
-//                 the PV product, rescales its O row in TMEM when m has to
-//                 move, and finally writes O = o/l and lse = m + ln l.
+//   warps 0-3     softmax of tile A; thread t owns query row t (TMEM lane t)
+//   warps 4-7     softmax of tile B
+//   warp 8        TMA producer: Q_A, Q_B once per unit, then K_j, V_j into a
+//                 ring of shared-memory slots (128-byte swizzle)
+//   warp 9        TMEM owner and MMA issuer (one thread)
+//   warps 10-11   no role; their warpgroup hands its registers to softmax
 //
-// The score and probability tiles live only in TMEM, registers and shared
-// memory; O is written to HBM once. This is the tiled forward of
-// "FlashAttention IO-aware tiling lab" ("Read each kernel phase": load Q,
-// score a K tile, update the online softmax, accumulate V, write O once) and
-// the recurrence of "IO-Aware Attention: Tiling the Score Matrix Without
-// Materializing It", section "Softmax over blocks, exactly". Causal tiles
-// beyond the diagonal are never loaded or computed and only tiles that
-// straddle it are masked (same page, section "Parallelism and the cost of
-// the split", last paragraph). Accumulation and rescaling are fp32 (same
-// page, section "Where the approach stops helping", last paragraph).
+// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A and O_B after
+// them (d columns each). S_X = Q_X K_j^T is one tcgen05.mma chain (M=128,
+// N=128) from shared memory; the softmax warps turn it into P_X =
+// 2^(scale*log2e*S_X - m) and store P_X as 16-bit back into the first 64
+// columns of S_X; O_X += P_X V_j then reads P from tensor memory and V from
+// shared memory. The issue order S_A(j), S_B(j), PV_A(j), S_A(j+1), PV_B(j),
+// S_B(j+1), ... keeps the tensor core busy on one tile while the other
+// tile's softmax runs (ping-pong), and the in-order execution of one
+// thread's tcgen05.mma makes every S_X(j+1) overwrite P_X(j) only after
+// PV_X(j) has read it.
 //
-// Differences from the pages' sketch, for sm_103a: accumulators live in
-// TMEM instead of registers/shared memory, so the 128 x d accumulator no
-// longer bounds the tile; the running max is moved lazily -- a row keeps its
-// old reference max until the new one exceeds it by 2^8 (in exp2 units), so
-// P stays <= 256 and the O rescale is rare. Because o and l share one
-// reference, o/l is unchanged: the result is still exact up to rounding.
+// Scores and probabilities never leave the chip; O is written to HBM once.
+// This is the tiled forward of "FlashAttention IO-aware tiling lab" ("Read
+// each kernel phase": load Q, score a K tile, update the online softmax,
+// accumulate V, write O once) with the recurrence of "IO-Aware Attention:
+// Tiling the Score Matrix Without Materializing It", section "Softmax over
+// blocks, exactly". Causal units stop their key loop at the diagonal and
+// only tiles crossing it are masked (same page, section "Parallelism and the
+// cost of the split", last paragraph). Accumulation and rescaling are fp32
+// (same page, section "Where the approach stops helping").
+//
+// sm_103a-specific choices: accumulators in TMEM (the 128 x d accumulator
+// does not bound the tile); a lazy running max -- a row keeps its reference
+// max until a new score exceeds it by 2^8, so P <= 256 and O is rarely
+// rescaled (o and l share the reference, so o/l is unchanged); packed fp32x2
+// arithmetic in the softmax; and an MMA issuer that builds its shared-memory
+// descriptors once and issues fully unrolled chains (a rolled loop with
+// per-MMA descriptor arithmetic made the single issuing thread, not the
+// tensor core, the bottleneck: ~83 vs ~45-64 cycles per MMA).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -48,36 +56,49 @@ namespace attn {
 
 namespace {
 
-constexpr int kBM = 128;       // query rows per tile (= TMEM lanes)
-constexpr int kBN = 128;       // keys per K/V tile
-constexpr int kSub = 128 * 128;  // bytes of one [128 rows][64 x 16-bit] swizzled sub-tile
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kBM = 128;          // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;          // keys per K/V tile
+constexpr int kSub = 128 * 128;   // bytes of one [128 rows][64 x 16-bit] swizzled sub-tile
+constexpr int kThreads = 384;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+// Register split (setmaxnreg): the launch gives 384 x 168 = 64512 registers;
+// the two softmax warpgroups take 200 each per thread and the control
+// warpgroup keeps 104: 2 x 128 x 200 + 128 x 104 = 64512 <= 64512.
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsControl = 104;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr float kRebaseLog2 = 8.0f;  // lazy rescale threshold (P <= 2^8)
 
 template <int D>
 struct Cfg {
-  static constexpr int STAGES = (D == 64) ? 3 : 2;
-  static constexpr int Q_BYTES = kBM * D * 2;
-  static constexpr int KV_BYTES = kBN * D * 2;
-  static constexpr int P_BYTES = kBM * kBN * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
-  // s_full[2], s_empty[2], p_full[2], p_empty[2], o_done, mma_done
-  static constexpr int N_BARS = 1 + 4 * STAGES + 8 + 2;
+  static constexpr int TILE_BYTES = kBM * D * 2;   // one Q, K or V tile
+  static constexpr int SLOTS = (D == 64) ? 10 : 5;
+  static constexpr int OFF_Q = 0;                  // Q_A, Q_B
+  static constexpr int OFF_RING = 2 * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + SLOTS * TILE_BYTES;
+  // q_full, q_empty, slot_full[S], slot_empty[S], s_full[2], p_full[2],
+  // o_full[2], o_empty[2], mma_done
+  static constexpr int N_BARS = 2 + 2 * SLOTS + 8 + 1;
   static constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+  // of every 8 column pairs, how many take the polynomial exp2 (the rest
+  // use the special-function unit). Measured on GB300: the special-function
+  // unit keeps up at both widths, so every pair uses it.
+  static constexpr int POLY_PAIRS_OF_8 = 0;
 };
+
+__host__ __device__ constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
+template <int D>
+__host__ __device__ constexpr uint32_t col_o(int x) {
+  return 256u + static_cast<uint32_t>(x) * static_cast<uint32_t>(D);
+}
 
 // Wait sites recorded in the status word on a timeout.
 enum : uint32_t {
-  kSiteProdKEmpty = 1, kSiteProdVEmpty, kSiteMmaQ, kSiteMmaK, kSiteMmaSEmpty, kSiteMmaV,
-  kSiteMmaP, kSiteSoftS, kSiteSoftPEmpty, kSiteSoftO, kSiteEpiO, kSiteMmaDone
+  kSiteProdQ = 1, kSiteProdSlot, kSiteMmaQ, kSiteMmaSlot, kSiteMmaP, kSiteMmaOEmpty,
+  kSiteSoftS, kSiteSoftO
 };
 
 template <bool BF16>
@@ -91,8 +112,52 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-// tcgen05.wait::ld that also ties the loaded registers to the wait, so no
-// use of them can be scheduled before the data has arrived.
+// 2^x on the FMA pipe for a pair of values: x = r + f with r = rint(x),
+// f in [-1/2, 1/2]; 2^f by a degree-3 polynomial with minimax relative
+// error 7.5e-5 on that interval (coefficients from a Remez exchange on the
+// relative error), and r added to the exponent field in the integer domain.
+// Packed fp32x2 arithmetic does two elements per instruction. x is clamped
+// at -125 (a result of 2^-125 stands in for 0: negligible against l >= 2^-8).
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 t = __fadd2_rn(x, make_float2(12582912.f, 12582912.f));  // 1.5 * 2^23
+  const float2 r = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));  // rint(x), exact
+  const float2 f = __ffma2_rn(r, make_float2(-1.f, -1.f), x);             // x - r, exact
+  float2 p = __ffma2_rn(make_float2(0.0551716685f, 0.0551716685f), f,
+                        make_float2(0.242611125f, 0.242611125f));
+  p = __ffma2_rn(p, f, make_float2(0.693260968f, 0.693260968f));
+  p = __ffma2_rn(p, f, make_float2(0.999928057f, 0.999928057f));
+  // t carries r in its low mantissa bits; shifting them to the exponent
+  // field and adding scales p by 2^r
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Four tcgen05.ld of 32 columns each, then one wait that is tied to all 128
+// registers so no use of them can be scheduled before the data arrives.
+__device__ __forceinline__ void tmem_ld_row128(uint32_t taddr, uint32_t (&r)[128]) {
+  ptx::tmem_ld_32x32b_x32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+  ptx::tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  ptx::tmem_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+  ptx::tmem_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+#define R8(b) "+r"(r[b]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), "+r"(r[b + 4]), \
+              "+r"(r[b + 5]), "+r"(r[b + 6]), "+r"(r[b + 7])
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : R8(0), R8(8), R8(16), R8(24), R8(32), R8(40), R8(48), R8(56), R8(64), R8(72),
+                 R8(80), R8(88), R8(96), R8(104), R8(112), R8(120)
+               :
+               : "memory");
+#undef R8
+}
+
+// tcgen05.wait::ld tied to 32 registers.
 __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.wait::ld.sync.aligned;"
@@ -115,67 +180,88 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// One work unit: query tiles A = rows [q0, q0+128) and B = [q0+128, q0+256)
+// of head bh, and how many key tiles each must see.
+struct Unit {
+  int bh, q0, rows_b, n_a, n_b, n_all;
+};
+
+__device__ __forceinline__ Unit unit_info(int u, int BH, int n_pairs, int T_q, int T_kv,
+                                          int causal) {
+  Unit w;
+  const int pair = n_pairs - 1 - u / BH;  // heaviest pairs first under a causal mask
+  w.bh = u % BH;
+  w.q0 = pair * 2 * kBM;
+  const int rows_a = min(kBM, T_q - w.q0);
+  w.rows_b = max(0, min(kBM, T_q - w.q0 - kBM));
+  const int n_kv = (T_kv + kBN - 1) / kBN;
+  const int off = T_kv - T_q;
+  const int last_a = w.q0 + rows_a - 1;
+  w.n_a = causal ? min(n_kv, (last_a + off + kBN) / kBN) : n_kv;
+  if (w.rows_b > 0) {
+    const int last_b = w.q0 + kBM + w.rows_b - 1;
+    w.n_b = causal ? min(n_kv, (last_b + off + kBN) / kBN) : n_kv;
+  } else {
+    w.n_b = 0;
+  }
+  w.n_all = max(w.n_a, w.n_b);
+  return w;
+}
+
+// Unit visited in round r by CTA bid of G: snake order over the heaviest-first
+// list, so that a CTA that took a heavy unit in one round takes a light one in
+// the next.
+__device__ __forceinline__ int unit_of_round(int r, int bid, int G) {
+  return (r & 1) ? r * G + (G - 1 - bid) : r * G + bid;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, void* __restrict__ out,
-                   float* __restrict__ lse, int T_q, int T_kv, int BH, int n_qtiles,
+                   float* __restrict__ lse, int T_q, int T_kv, int BH, int n_pairs,
                    float scale_log2, int causal, unsigned int* __restrict__ status) {
   using C = Cfg<D>;
-  constexpr int ST = C::STAGES;
+  constexpr int SL = C::SLOTS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + ST;
-  uint64_t* v_full = k_empty + ST;
-  uint64_t* v_empty = v_full + ST;
-  uint64_t* s_full = v_empty + ST;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 2;
-  uint64_t* o_done = p_empty + 2;
-  uint64_t* mma_done = o_done + 1;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* slot_full = bars + 2;
+  uint64_t* slot_empty = slot_full + SL;
+  uint64_t* s_full = slot_empty + SL;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = p_full + 2;
+  uint64_t* o_empty = o_full + 2;
+  uint64_t* mma_done = o_empty + 2;
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMPTR);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // Heaviest query tiles first (largest index under a causal mask), all
-  // heads of one tile index before the next: the block scheduler then hands
-  // out the long tiles early and the short ones fill the tail.
-  const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int q0 = qt * kBM;
+  const int U = n_pairs * BH;
+  const int G = static_cast<int>(gridDim.x);
+  const int bid = static_cast<int>(blockIdx.x);
   const int off = T_kv - T_q;
-  int kv_end = T_kv;
-  if (causal) {
-    const int last_row = min(q0 + kBM - 1, T_q - 1);
-    kv_end = min(T_kv, last_row + off + 1);
-  }
-  const int n_kv = (kv_end + kBN - 1) / kBN;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    for (int i = 0; i < ST; ++i) {
-      ptx::mbar_init(&k_full[i], 1);
-      ptx::mbar_init(&k_empty[i], 1);
-      ptx::mbar_init(&v_full[i], 1);
-      ptx::mbar_init(&v_empty[i], 1);
+    ptx::mbar_init(q_empty, 1);
+    for (int i = 0; i < SL; ++i) {
+      ptx::mbar_init(&slot_full[i], 1);
+      ptx::mbar_init(&slot_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&s_full[i], 1);
-      ptx::mbar_init(&s_empty[i], 128);
-      ptx::mbar_init(&p_full[i], 128);
-      ptx::mbar_init(&p_empty[i], 1);
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(&s_full[x], 1);
+      ptx::mbar_init(&p_full[x], 128);
+      ptx::mbar_init(&o_full[x], 1);
+      ptx::mbar_init(&o_empty[x], 128);
     }
-    ptx::mbar_init(o_done, 1);
     ptx::mbar_init(mma_done, 1);
     ptx::fence_mbarrier_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     ptx::tmem_alloc(tmem_ptr, C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -184,246 +270,313 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
 
-  const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
-  const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
-  const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
-  const uint32_t sP = ptx::smem_u32(smem + C::OFF_P);
+  // Each setmaxnreg sits in the branch of the role code it serves, so the
+  // compiler applies its register limit to exactly that code.
+  if (warp >= 8) {
+    // one setmaxnreg instruction for the whole control warpgroup (.aligned)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    if (warp == kWarpProducer) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&tmQ);
+        ptx::prefetch_tensormap(&tmK);
+        ptx::prefetch_tensormap(&tmV);
+        const uint64_t pol_kv = ptx::policy_evict_last();
+        const uint64_t pol_q = ptx::policy_evict_first();
+        uint32_t g = 0;   // ring fills issued
+        uint32_t nq = 0;  // Q loads issued
+        bool ok = true;
+        for (int r = 0; ok && r * G < U; ++r) {
+          const int u = unit_of_round(r, bid, G);
+          if (u >= U) continue;
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal);
+          ok = ptx::mbar_wait(q_empty, (nq & 1) ^ 1, status, status_word(kKernPrefill, kSiteProdQ));
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(q_full, C::TILE_BYTES * (w.rows_b > 0 ? 2 : 1));
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            ptx::tma_load_3d(smem + C::OFF_Q + c * kSub, &tmQ, q_full, c * 64, w.q0, w.bh, pol_q);
+            if (w.rows_b > 0)
+              ptx::tma_load_3d(smem + C::OFF_Q + C::TILE_BYTES + c * kSub, &tmQ, q_full, c * 64,
+                               w.q0 + kBM, w.bh, pol_q);
+          }
+          ++nq;
+          for (int j = 0; ok && j < w.n_all; ++j) {
+#pragma unroll
+            for (int kind = 0; kind < 2; ++kind) {  // K_j, then V_j
+              const uint32_t slot = g % SL;
+              ok = ptx::mbar_wait(&slot_empty[slot], ((g / SL) & 1) ^ 1, status,
+                                  status_word(kKernPrefill, kSiteProdSlot));
+              if (!ok) break;
+              ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
+              uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c)
+                ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot], c * 64,
+                                 j * kBN, w.bh, pol_kv);
+              ++g;
+            }
+          }
+        }
+        if (!ok) {
+          // Error path: let the copies in flight land before the CTA (and its
+          // shared memory) goes away. Only the last SLOTS fills and the last
+          // Q load can still be outstanding.
+          if (nq > 0) mbar_drain(q_full, (nq - 1) & 1);
+          for (uint32_t i = (g > SL ? g - SL : 0); i < g; ++i)
+            mbar_drain(&slot_full[i % SL], (i / SL) & 1);
+        }
+      }
+    } else if (warp == kWarpMma) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kBM, kBN, false, false);
+        constexpr uint32_t idO = ptx::make_idesc_f16(BF16, kBM, D, false, true);
+        const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
+        const uint32_t sRing = ptx::smem_u32(smem + C::OFF_RING);
+        uint32_t g = 0, nq = 0;
+        uint32_t np[2] = {0, 0}, noe[2] = {0, 0};
+        bool ok = true;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      ptx::prefetch_tensormap(&tmQ);
-      ptx::prefetch_tensormap(&tmK);
-      ptx::prefetch_tensormap(&tmV);
-      const uint64_t pol_kv = ptx::policy_evict_last();
-      const uint64_t pol_q = ptx::policy_evict_first();
-      ptx::mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        ptx::tma_load_3d(smem + C::OFF_Q + c * kSub, &tmQ, q_full, c * 64, q0, bh, pol_q);
-      int k_issued = 0, v_issued = 0;
-      bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % ST;
-        const uint32_t ph = (j / ST) & 1;
-        ok = ptx::mbar_wait(&k_empty[st], ph ^ 1, status, status_word(kKernPrefill, kSiteProdKEmpty));
-        if (!ok) break;
-        ptx::mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          ptx::tma_load_3d(smem + C::OFF_K + st * C::KV_BYTES + c * kSub, &tmK, &k_full[st],
-                           c * 64, j * kBN, bh, pol_kv);
-        k_issued = j + 1;
-        ok = ptx::mbar_wait(&v_empty[st], ph ^ 1, status, status_word(kKernPrefill, kSiteProdVEmpty));
-        if (!ok) break;
-        ptx::mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          ptx::tma_load_3d(smem + C::OFF_V + st * C::KV_BYTES + c * kSub, &tmV, &v_full[st],
-                           c * 64, j * kBN, bh, pol_kv);
-        v_issued = j + 1;
-      }
-      if (!ok) {
-        // Error path: let the copies already in flight land before the CTA
-        // (and its shared memory) goes away. Only the last STAGES loads of
-        // each ring can still be outstanding.
-        mbar_drain(q_full, 0);
-        for (int j = max(0, k_issued - ST); j < k_issued; ++j) mbar_drain(&k_full[j % ST], (j / ST) & 1);
-        for (int j = max(0, v_issued - ST); j < v_issued; ++j) mbar_drain(&v_full[j % ST], (j / ST) & 1);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kBM, kBN, false, false);
-      constexpr uint32_t idO = ptx::make_idesc_f16(BF16, kBM, D, false, true);
-      bool ok = ptx::mbar_wait(q_full, 0, status, status_word(kKernPrefill, kSiteMmaQ));
-      for (int j = 0; j <= n_kv && ok; ++j) {
-        if (j < n_kv) {
-          const int st = j % ST;
-          const int sb = j & 1;
-          ok = ptx::mbar_wait(&k_full[st], (j / ST) & 1, status, status_word(kKernPrefill, kSiteMmaK));
-          if (!ok) break;
-          ok = ptx::mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, status,
-                              status_word(kKernPrefill, kSiteMmaSEmpty));
-          if (!ok) break;
-          ptx::tc_fence_after();
-          const uint32_t kbase = sK + st * C::KV_BYTES;
+        auto wait_slot = [&](uint32_t idx) {
+          return ptx::mbar_wait(&slot_full[idx % SL], (idx / SL) & 1, status,
+                                status_word(kKernPrefill, kSiteMmaSlot));
+        };
+        const uint64_t desc_q0 = ptx::make_sdesc_sw128(sQ, 16, 1024);
+        const uint64_t desc_k0 = ptx::make_sdesc_sw128(sRing, 16, 1024);
+        const uint64_t desc_v0 = ptx::make_sdesc_sw128(sRing, kSub, 1024);
+        auto issue_s = [&](int x, uint32_t kslot) {
+          const uint64_t qd = desc_q0 + ((x * C::TILE_BYTES) >> 4);
+          const uint64_t kd = desc_k0 + ((kslot * C::TILE_BYTES) >> 4);
+          const uint32_t d_s = tmem + col_s(x);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * kSub + (kk & 3) * 32;
-            const uint64_t a = ptx::make_sdesc_sw128(sQ + koff, 16, 1024);
-            const uint64_t b = ptx::make_sdesc_sw128(kbase + koff, 16, 1024);
-            ptx::mma_f16_ss(tmem + (sb ? C::COL_S1 : C::COL_S0), a, b, idS, kk > 0);
+            ptx::mma_f16_ss(d_s, qd + (koff >> 4), kd + (koff >> 4), idS, kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(&s_full[sb]);
-          ptx::mma_commit(&k_empty[st]);
-        }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int st = jj % ST;
-          const int pb = jj & 1;
-          ok = ptx::mbar_wait(&v_full[st], (jj / ST) & 1, status, status_word(kKernPrefill, kSiteMmaV));
+          ptx::mma_commit(&s_full[x]);
+        };
+        auto issue_pv = [&](int x, uint32_t vslot, bool first) {
+          const uint64_t vd = desc_v0 + ((vslot * C::TILE_BYTES) >> 4);
+          const uint32_t d_o = tmem + col_o<D>(x);
+          const uint32_t a_p = tmem + col_s(x);
+          const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            ptx::mma_f16_ts(d_o, a_p + kk * 8, vd + ((kk * 16 * 128) >> 4), idO, kk > 0 ? 1u : acc0);
+        };
+        auto wait_p = [&](int x, bool first) {
+          bool good = ptx::mbar_wait(&p_full[x], np[x] & 1, status,
+                                     status_word(kKernPrefill, kSiteMmaP));
+          ++np[x];
+          if (good && first) {
+            // O_X is overwritten by this unit's first product: the previous
+            // unit's epilogue must have read it.
+            good = ptx::mbar_wait(&o_empty[x], (noe[x] & 1) ^ 1, status,
+                                  status_word(kKernPrefill, kSiteMmaOEmpty));
+            ++noe[x];
+          }
+          ptx::tc_fence_after();
+          return good;
+        };
+
+        for (int r = 0; ok && r * G < U; ++r) {
+          const int u = unit_of_round(r, bid, G);
+          if (u >= U) continue;
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal);
+          ok = ptx::mbar_wait(q_full, nq & 1, status, status_word(kKernPrefill, kSiteMmaQ));
+          ++nq;
           if (!ok) break;
-          ok = ptx::mbar_wait(&p_full[pb], (jj >> 1) & 1, status, status_word(kKernPrefill, kSiteMmaP));
+          // prologue: both score tiles of key tile 0
+          ok = wait_slot(g);
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint32_t vbase = sV + st * C::KV_BYTES;
-          const uint32_t pbase = sP + pb * C::P_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t a =
-                ptx::make_sdesc_sw128(pbase + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = ptx::make_sdesc_sw128(vbase + kk * 16 * 128, kSub, 1024);
-            ptx::mma_f16_ss(tmem + C::COL_O, a, b, idO, (jj > 0 || kk > 0) ? 1u : 0u);
+          issue_s(0, g % SL);
+          if (w.n_b > 0) issue_s(1, g % SL);
+          ptx::mma_commit(&slot_empty[g % SL]);
+          if (w.n_all == 1) ptx::mma_commit(q_empty);
+          for (int j = 0; j < w.n_all; ++j) {
+            const uint32_t vi = g + 2 * j + 1;  // V_j
+            const uint32_t ki = vi + 1;         // K_{j+1}
+            ok = wait_slot(vi);
+            if (!ok) break;
+            if (j < w.n_a) {
+              ok = wait_p(0, j == 0);
+              if (!ok) break;
+              issue_pv(0, vi % SL, j == 0);
+              if (j == w.n_a - 1) ptx::mma_commit(&o_full[0]);
+            }
+            if (j + 1 < w.n_all) {
+              ok = wait_slot(ki);
+              if (!ok) break;
+              ptx::tc_fence_after();
+              if (j + 1 < w.n_a) issue_s(0, ki % SL);
+            }
+            if (j < w.n_b) {
+              ok = wait_p(1, j == 0);
+              if (!ok) break;
+              issue_pv(1, vi % SL, j == 0);
+              if (j == w.n_b - 1) ptx::mma_commit(&o_full[1]);
+            }
+            ptx::mma_commit(&slot_empty[vi % SL]);
+            if (j + 1 < w.n_all) {
+              if (j + 1 < w.n_b) issue_s(1, ki % SL);
+              ptx::mma_commit(&slot_empty[ki % SL]);
+              if (j + 2 == w.n_all) ptx::mma_commit(q_empty);
+            }
           }
-          ptx::mma_commit(o_done);
-          ptx::mma_commit(&v_empty[st]);
-          ptx::mma_commit(&p_empty[pb]);
+          g += 2 * w.n_all;
         }
+        // All MMAs this thread issued must be complete before TMEM is freed.
+        ptx::mma_commit(mma_done);
+        mbar_drain(mma_done, 0);
       }
-      // All MMAs this thread issued must be complete before TMEM is freed.
-      ptx::mma_commit(mma_done);
-      mbar_drain(mma_done, 0);
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;               // TMEM lanes [32*quarter, 32*quarter+32)
-    const int r = quarter * 32 + lane;          // row within the tile
-    const int row = q0 + r;                     // absolute query row
-    const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int last_key = causal ? min(T_kv - 1, row + off) : T_kv - 1;
-    float m_used = -INFINITY;  // reference max, log2 units of the scaled score
-    float l = 0.f;
+    const int x = warp >> 2;                   // 0 = tile A, 1 = tile B
+    const int quarter = warp & 3;              // TMEM lanes [32*quarter, 32*quarter+32)
+    const int r = quarter * 32 + lane;         // row within the tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t t_s = t_lane + col_s(x);
+    const uint32_t t_o = t_lane + col_o<D>(x);
+    uint32_t ns = 0, no = 0;
     bool ok = true;
-    uint8_t* prow_base = smem + C::OFF_P + r * 128;
-    const int rsw = r & 7;
 
-    for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      const int pb = j & 1;
-      ok = ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, status, status_word(kKernPrefill, kSiteSoftS));
-      // tcgen05.ld/st/wait are warp-collective (.sync.aligned): every branch
-      // around them must be taken by the whole warp.
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      float s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t raw[32];
-        ptx::tmem_ld_32x32b_x32(t_row + (sb ? C::COL_S1 : C::COL_S0) + c * 32, raw);
-        tmem_wait_ld_regs(raw);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&s_empty[sb]);
+    for (int rr = 0; ok && rr * G < U; ++rr) {
+      const int u = unit_of_round(rr, bid, G);
+      if (u >= U) continue;
+      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal);
+      const int n_x = x ? w.n_b : w.n_a;
+      if (n_x == 0) continue;
+      const int row = w.q0 + x * kBM + r;        // absolute query row
+      const int last_key = causal ? min(T_kv - 1, row + off) : T_kv - 1;
+      float m_used = -INFINITY;  // reference max, log2 units of the scaled score
+      float l = 0.f;
 
-      const int key0 = j * kBN;
-      if (key0 + kBN - 1 > last_key) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (key0 + c > last_key) s[c] = -INFINITY;
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_tile = mx * scale_log2;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (m_tile > m_used + kRebaseLog2) {
-        alpha = ptx::ex2_approx(m_used - m_tile);   // 0 when m_used = -inf
-        rescale = (m_used != -INFINITY);
-        l *= alpha;
-        m_used = m_tile;
-      }
-      const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-
-      ok = ptx::mbar_wait(&p_empty[pb], ((j >> 1) & 1) ^ 1, status,
-                          status_word(kKernPrefill, kSiteSoftPEmpty));
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      float rs = 0.f;
-      uint8_t* prow = prow_base + pb * C::P_BYTES;
-#pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = ptx::ex2_approx(fmaf(s[c * 8 + i], scale_log2, -m_ref));
-          rs += p[i];
-        }
-        uint4 w;
-        w.x = pack2<BF16>(p[0], p[1]);
-        w.y = pack2<BF16>(p[2], p[3]);
-        w.z = pack2<BF16>(p[4], p[5]);
-        w.w = pack2<BF16>(p[6], p[7]);
-        const int sub = c >> 3;   // keys 0-63 / 64-127
-        const int chunk = (c & 7) ^ rsw;
-        *reinterpret_cast<uint4*>(prow + sub * kSub + (chunk << 4)) = w;
-      }
-      l += rs;
-      ptx::fence_proxy_async_smem();
-
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O holds the sum through tile j-1; wait for that product, then
-        // multiply this warp's rows of O by their alpha in place (rows that
-        // keep their reference max have alpha = 1).
-        ok = ptx::mbar_wait(o_done, (j - 1) & 1, status, status_word(kKernPrefill, kSiteSoftO));
+      for (int j = 0; j < n_x; ++j) {
+        ok = ptx::mbar_wait(&s_full[x], ns & 1, status, status_word(kKernPrefill, kSiteSoftS));
+        ++ns;
+        // tcgen05.ld/st/wait are warp-collective (.sync.aligned): every
+        // branch around them must be taken by the whole warp.
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-        const float mul = rescale ? alpha : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t raw[32];
-          ptx::tmem_ld_32x32b_x32(t_row + C::COL_O + c * 32, raw);
-          tmem_wait_ld_regs(raw);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * mul);
-          ptx::tmem_st_32x32b_x32(t_row + C::COL_O + c * 32, raw);
-        }
-        ptx::tmem_wait_st();
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&p_full[pb]);
-    }
+        uint32_t sr[128];
+        tmem_ld_row128(t_s, sr);
+        float* s = reinterpret_cast<float*>(sr);
 
-    // ------------------------------------------------------------ epilogue
-    if (ok) ok = ptx::mbar_wait(o_done, (n_kv - 1) & 1, status, status_word(kKernPrefill, kSiteEpiO));
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+        const int key0 = j * kBN;
+        if (key0 + kBN - 1 > last_key) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (key0 + c > last_key) s[c] = -INFINITY;
+        }
+        // row max: four independent chains of 3-input max
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kBN; c += 8) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        }
+        const float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+        const float m_tile = mx * scale_log2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_tile > m_used + kRebaseLog2) {
+          alpha = ptx::ex2_approx(m_used - m_tile);  // 0 when m_used = -inf
+          rescale = (m_used != -INFINITY);
+          l *= alpha;
+          m_used = m_tile;
+        }
+        const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+
+        // p = 2^(s * scale * log2e - m_ref), two columns per instruction
+        const float2 sl2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_ref, -m_ref);
+        float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};  // four independent sum chains
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float2 xx = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, nm2);
+          float2 pp;
+          if (((c >> 1) & 7) < C::POLY_PAIRS_OF_8) {
+            pp = exp2_poly2(xx);
+          } else {
+            pp.x = ptx::ex2_approx(xx.x);
+            pp.y = ptx::ex2_approx(xx.y);
+          }
+          rs2[(c >> 1) & 3] = __fadd2_rn(rs2[(c >> 1) & 3], pp);
+          pk[c >> 1] = pack2<BF16>(pp.x, pp.y);
+        }
+        const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+        l += rsa.x + rsa.y;
+
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O_X holds the sum through key tile j-1 (that product is complete:
+          // it was issued before S_X(j), whose completion this warp waited
+          // for). Multiply this warp's rows by their alpha in place; rows
+          // that keep their reference max multiply by 1.
+          const float mul = rescale ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t raw[32];
+            ptx::tmem_ld_32x32b_x32(t_o + c * 32, raw);
+            tmem_wait_ld_regs(raw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * mul);
+            ptx::tmem_st_32x32b_x32(t_o + c * 32, raw);
+          }
+        }
+        // P_X (16-bit pairs) into the first 64 columns of S_X
+        ptx::tmem_st_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        ptx::tmem_st_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&p_full[x]);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      ok = ptx::mbar_wait(&o_full[x], no & 1, status, status_word(kKernPrefill, kSiteSoftO));
+      ++no;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       ptx::tc_fence_after();
       const float inv_l = 1.f / l;
       const bool write = row < T_q;
       uint8_t* orow = reinterpret_cast<uint8_t*>(out) +
-                      (static_cast<size_t>(bh) * T_q + (write ? row : 0)) * D * 2;
+                      (static_cast<size_t>(w.bh) * T_q + (write ? row : 0)) * D * 2;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t raw[32];
-        ptx::tmem_ld_32x32b_x32(t_row + C::COL_O + c * 32, raw);
+        ptx::tmem_ld_32x32b_x32(t_o + c * 32, raw);
         tmem_wait_ld_regs(raw);
         if (write) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 w;
-            w.x = pack2<BF16>(__uint_as_float(raw[g * 8 + 0]) * inv_l, __uint_as_float(raw[g * 8 + 1]) * inv_l);
-            w.y = pack2<BF16>(__uint_as_float(raw[g * 8 + 2]) * inv_l, __uint_as_float(raw[g * 8 + 3]) * inv_l);
-            w.z = pack2<BF16>(__uint_as_float(raw[g * 8 + 4]) * inv_l, __uint_as_float(raw[g * 8 + 5]) * inv_l);
-            w.w = pack2<BF16>(__uint_as_float(raw[g * 8 + 6]) * inv_l, __uint_as_float(raw[g * 8 + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + (c * 32 + g * 8) * 2) = w;
+          for (int g8 = 0; g8 < 4; ++g8) {
+            uint4 v;
+            const float* f = reinterpret_cast<const float*>(&raw[g8 * 8]);
+            v.x = pack2<BF16>(f[0] * inv_l, f[1] * inv_l);
+            v.y = pack2<BF16>(f[2] * inv_l, f[3] * inv_l);
+            v.z = pack2<BF16>(f[4] * inv_l, f[5] * inv_l);
+            v.w = pack2<BF16>(f[6] * inv_l, f[7] * inv_l);
+            *reinterpret_cast<uint4*>(orow + (c * 32 + g8 * 8) * 2) = v;
           }
         }
       }
       if (write)
-        lse[static_cast<size_t>(bh) * T_q + row] = (m_used + __log2f(l)) * 0.69314718055994531f;
+        lse[static_cast<size_t>(w.bh) * T_q + row] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&o_empty[x]);
     }
     ptx::tc_fence_before();
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -467,6 +620,20 @@ bool make_map(CUtensorMap* map, const void* base, int T, int BH, int D, bool bf1
   return r == CUDA_SUCCESS;
 }
 
+int device_sms(int dev) {
+  static std::mutex mu;
+  static int sms[64] = {};
+  if (dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> g(mu);
+  if (!sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
 template <int D, bool BF16>
 cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
   using C = Cfg<D>;
@@ -490,10 +657,13 @@ cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
       !make_map(&mv, p.v, p.T_kv, BH, D, BF16))
     return cudaErrorInvalidValue;
   const int n_qtiles = (p.T_q + kBM - 1) / kBM;
+  const int n_pairs = (n_qtiles + 1) / 2;
+  const long long units = static_cast<long long>(n_pairs) * BH;
+  const int sms = device_sms(dev);
+  const int grid = static_cast<int>(units < sms ? units : sms);
   const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-  dim3 grid(static_cast<unsigned>(n_qtiles) * static_cast<unsigned>(BH));
-  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p.o, p.lse, p.T_q, p.T_kv, BH,
-                                                  n_qtiles, scale_log2, p.causal, p.status);
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p.o, p.lse, p.T_q, p.T_kv, BH, n_pairs,
+                                                  scale_log2, p.causal, p.status);
   return cudaGetLastError();
 }
 
