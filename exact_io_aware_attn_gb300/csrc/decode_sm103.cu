@@ -17,7 +17,9 @@
 //                          (m, l, o) in fp32 and writes it to the workspace.
 //   decode_combine_kernel  one warp per (b, h): M = max m_s,
 //                          w_s = 2^(m_s - M), L = sum w_s l_s,
-//                          O = sum w_s o_s / L, lse = (M + log2 L) ln 2.
+//                          O = sum w_s o_s / L, lse = (M + log2 L) ln 2;
+//                          launched as a programmatic dependent of the split
+//                          kernel, so its launch overlaps the split's tail.
 //
 // Inside a partition, groups of d/8 threads share one key (each thread owns
 // 8 of the d dimensions, one 16-byte load); a warp reads consecutive keys,
@@ -201,6 +203,11 @@ __global__ void __launch_bounds__(kDecThreads)
     *reinterpret_cast<float4*>(part + sub * 8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
     if (lane == 0) *reinterpret_cast<float4*>(part + D) = make_float4(m, l, 0.f, 0.f);
   }
+  // The merge kernel is launched as a programmatic dependent of this grid:
+  // once every CTA has passed this point (or exited) it may be scheduled, and
+  // it waits (griddepcontrol.wait) for this grid's completion and memory
+  // flush before reading any partial.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <int D, bool BF16>
@@ -208,6 +215,8 @@ __global__ void __launch_bounds__(128)
     decode_combine_kernel(const float* __restrict__ ws, uint8_t* __restrict__ out,
                           float* __restrict__ lse, int BH, int S) {
   constexpr int PER = D / 32;   // dims per lane
+  // wait for the split grid (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x * 4 + warp;
@@ -215,6 +224,7 @@ __global__ void __launch_bounds__(128)
   const size_t stride = decode_partial_floats(D);
   const float* part = ws + static_cast<size_t>(bh) * S * stride;
 
+  // each lane reads the (m, l) of partitions lane, lane+32, ... at once
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, part[s * stride + D]);
 #pragma unroll
@@ -224,14 +234,27 @@ __global__ void __launch_bounds__(128)
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float* ps = part + s * stride;
-    const float ms = ps[D];
-    const float w = (ms == -INFINITY) ? 0.f : ex2f(ms - M);
-    L = fmaf(w, ps[D + 1], L);
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s_mine = s0 + lane;
+    float w_mine = 0.f;
+    if (s_mine < S) {
+      const float ms = part[s_mine * stride + D];
+      w_mine = (ms == -INFINITY) ? 0.f : ex2f(ms - M);
+      L = fmaf(w_mine, part[s_mine * stride + D + 1], L);
+    }
+    const int n = min(32, S - s0);
+    // weights broadcast from the lane that computed them; the o loads of
+    // different partitions are independent and overlap
+#pragma unroll 8
+    for (int t = 0; t < n; ++t) {
+      const float w = __shfl_sync(0xffffffffu, w_mine, t);
+      const float* ps = part + (s0 + t) * stride + lane * PER;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, ps[lane * PER + i], acc[i]);
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, ps[i], acc[i]);
+    }
   }
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) L += __shfl_xor_sync(0xffffffffu, L, w);
   const float inv = 1.f / L;
   uint8_t* orow = out + static_cast<size_t>(bh) * D * 2 + lane * PER * 2;
   if constexpr (PER == 2) {
@@ -272,9 +295,20 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* ws, cudaStream_t stream)
       static_cast<const uint8_t*>(p.v), ws, p.T_kv, S, chunk, scale_log2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 g2(static_cast<unsigned>((BH + 3) / 4));
-  decode_combine_kernel<D, BF16><<<g2, 128, 0, stream>>>(ws, static_cast<uint8_t*>(p.o), p.lse, BH, S);
-  return cudaGetLastError();
+  // the merge is a programmatic dependent launch: it may start while the
+  // split grid drains and waits for it on the device (griddepcontrol.wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((BH + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>, static_cast<const float*>(ws),
+                            static_cast<uint8_t*>(p.o), p.lse, BH, S);
 }
 
 }  // namespace
