@@ -37,6 +37,7 @@ SIGNATURES = {
     "attn_abi_version": (_I, []),
     "attn_last_kernel_name": (ctypes.c_char_p, []),
     "attn_fwd_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP]),
+    "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _VP]),
 }
 
 # Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
@@ -97,6 +98,12 @@ def get_device_error(stream=None):
     word = ctypes.c_uint(0)
     st = lib().attn_get_device_error(_stream_ptr(stream), ctypes.byref(word))
     return int(st), int(word.value)
+
+
+def selftest_wait_timeout(limit_us, stream=None) -> int:
+    """Enqueue the failure-detection self-test (a bounded wait that runs
+    out after limit_us); returns the status of the enqueue."""
+    return int(lib().attn_selftest_wait_timeout(int(limit_us), _stream_ptr(stream)))
 
 
 def _stream_ptr(stream):

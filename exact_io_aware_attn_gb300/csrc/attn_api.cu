@@ -12,11 +12,25 @@
 #include "attn.h"
 #include "attn_internal.h"
 #include "attn_status.h"
+#include "ptx_sm103.cuh"
 
 namespace {
 
 // One status word per device (each device's module instance has its own).
 __device__ unsigned int g_status_word;
+
+// Failure-detection self-test: one thread waits on an mbarrier that nothing
+// will ever complete, with the same bounded wait the attention kernels use
+// but a short limit. The wait gives up, records the timeout in the status
+// word and the kernel returns; nothing faults or hangs.
+__global__ void selftest_wait_kernel(unsigned int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    attn::ptx::mbar_init(&bar, 1);
+    attn::ptx::fence_mbarrier_init();
+    attn::ptx::mbar_wait_for(&bar, 0, status, attn::status_word(attn::kKernSelftest, 1), limit_ns);
+  }
+}
 
 unsigned int* status_ptr() {
   static std::mutex mu;
@@ -259,6 +273,15 @@ const char* attn_status_string(int status) {
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 2000000u) return ATTN_ERR_INVALID_ARG;
+  unsigned int* st = status_ptr();
+  if (!st) return ATTN_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      st, static_cast<unsigned long long>(limit_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
 const char* attn_last_kernel_name(void) { return t_last_kernel; }
 

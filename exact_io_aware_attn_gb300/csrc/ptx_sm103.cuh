@@ -58,12 +58,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return done != 0;
 }
 
-// Bounded wait for the phase of parity `parity` to complete. Spins; after a
-// limit measured on the global timer (or as soon as another thread of the
-// grid has recorded an error) it records `code` in *status (first error
-// wins) and returns false, so no wait can hang the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
-                                          uint32_t code) {
+// Bounded wait for the phase of parity `parity` to complete. Spins; after
+// `limit_ns` on the global timer (or as soon as another thread of the grid
+// has recorded an error) it records `code` in *status (first error wins) and
+// returns false, so no wait can hang the GPU.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
+                                              unsigned int* status, uint32_t code,
+                                              uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -72,12 +73,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     if (mbar_try_wait(a, parity)) return true;
     if ((++spins & 255u) == 0) {
       if (*reinterpret_cast<volatile unsigned int*>(status) != 0u) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicCAS(status, 0u, code);
         return false;
       }
     }
   }
+}
+
+// The kernels' wait: the library-wide limit kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          uint32_t code) {
+  return mbar_wait_for(bar, parity, status, code, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------------------------

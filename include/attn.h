@@ -134,6 +134,19 @@ int attn_decode_num_splits(int B, int h, int T_kv, int d);
  */
 attn_status_t attn_get_device_error(void* stream, unsigned int* site);
 
+/*
+ * attn_selftest_wait_timeout -- tests the failure-detection path without
+ * faulting the GPU. Enqueues on `stream` a one-thread kernel that waits on a
+ * device barrier nothing will complete, using the same bounded wait as the
+ * attention kernels but with a limit of `limit_us` microseconds (1 ..
+ * 2,000,000). The wait gives up, the kernel records ATTN_ERR_TIMEOUT (kernel
+ * id 4, site 1) in the device status word unless an error is already
+ * recorded, and returns; a following attn_get_device_error reports and
+ * clears it, and the context stays usable. Returns ATTN_ERR_INVALID_ARG for
+ * a limit out of range, ATTN_OK once enqueued.
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
 /* attn_status_string -- static, NUL-terminated name of a status code. */
 const char* attn_status_string(int status);
 

@@ -174,3 +174,8 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libattn.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.lib()
+
+
+def test_selftest_limit_validated_before_launch(L):
+    assert _lib.selftest_wait_timeout(0) == _lib.ATTN_ERR_INVALID_ARG
+    assert _lib.selftest_wait_timeout(2000001) == _lib.ATTN_ERR_INVALID_ARG
