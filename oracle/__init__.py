@@ -5,6 +5,7 @@ product path."""
 
 from .oracle import (  # noqa: F401
     causal_visible,
+    gqa_attention,
     merge_partials,
     online_attention,
     online_softmax_states,

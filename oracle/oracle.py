@@ -55,6 +55,7 @@ __all__ = [
     "merge_partials",
     "split_kv_attention",
     "causal_visible",
+    "gqa_attention",
 ]
 
 
@@ -255,3 +256,32 @@ def merge_partials(ms, ls, os_):
 def split_kv_attention(q, k, v, num_splits, scale=None):
     """Split-KV attention of one query row: partials then exact merge."""
     return merge_partials(*split_partials(q, k, v, num_splits, scale=scale))
+
+
+def gqa_attention(q, k, v, scale=None, causal=False, rows=None):
+    """Grouped-query attention, float64: returns (O, lse).
+
+    q: [B, h_q, T_q, d]; k, v: [B, h_kv, T_kv, d] with h_q a multiple of
+    h_kv. Query head i attends with key/value head i // (h_q // h_kv): a group
+    of h_q/h_kv query heads shares one cached key/value head ("Attention and
+    Its Computational Cost", section "The other shape: one query, many keys":
+    grouped-query attention reduces the number of key and value heads and so
+    the factor of h in the cache read). Each query head is then plain
+    standard_attention against its key/value head.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be [B, h, T, d]")
+    h_q, h_kv = q.shape[1], k.shape[1]
+    if h_kv < 1 or h_q % h_kv != 0:
+        raise ValueError("h_q must be a positive multiple of h_kv")
+    group = h_q // h_kv
+    outs, lses = [], []
+    for i in range(h_q):
+        o, l = standard_attention(q[:, i], k[:, i // group], v[:, i // group], scale=scale,
+                                  causal=causal, rows=rows)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs, axis=1), np.stack(lses, axis=1)

@@ -37,6 +37,7 @@ def real_oracle():
         split_partials=oracle.split_partials,
         merge_partials=oracle.merge_partials,
         split_kv_attention=oracle.split_kv_attention,
+        gqa_attention=oracle.gqa_attention,
     )
 
 
@@ -250,6 +251,43 @@ def check_split_merge(impl):
     return fails
 
 
+def check_gqa(impl):
+    """Grouped-query attention against the library's float64 grouped SDPA,
+    and its reductions: one query head per key/value head is standard
+    attention; repeating each key/value head `group` times is the same."""
+    import torch
+    import torch.nn.functional as F
+    fails = []
+    rng = _rng(7)
+    for (b, h_q, h_kv, t_q, t_kv, d) in ((2, 4, 2, 5, 9, 8), (1, 8, 2, 1, 33, 16), (1, 6, 3, 7, 7, 4)):
+        q = rng.standard_normal((b, h_q, t_q, d))
+        k = rng.standard_normal((b, h_kv, t_kv, d))
+        v = rng.standard_normal((b, h_kv, t_kv, d))
+        for causal in (False, True):
+            if causal and t_q > t_kv:
+                continue
+            mask = (torch.ones(t_q, t_kv, dtype=torch.bool).tril(diagonal=t_kv - t_q)
+                    if causal else None)
+            o_lib = F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(k),
+                                                   torch.from_numpy(v), attn_mask=mask,
+                                                   enable_gqa=True).numpy()
+            o, lse = impl.gqa_attention(q, k, v, causal=causal)
+            if not _close(o, o_lib, rtol=1e-10, atol=1e-12):
+                fails.append(f"gqa vs library shape={(b, h_q, h_kv, t_q, t_kv, d)} causal={causal}")
+            g = h_q // h_kv
+            o_rep, lse_rep = impl.standard_attention(q, np.repeat(k, g, axis=1),
+                                                     np.repeat(v, g, axis=1), causal=causal)
+            if not (_close(o, o_rep) and _close(lse, lse_rep)):
+                fails.append(f"gqa vs repeated heads shape={(b, h_q, h_kv)} causal={causal}")
+    q = rng.standard_normal((1, 3, 4, 8))
+    k = rng.standard_normal((1, 3, 6, 8))
+    o1, l1 = impl.gqa_attention(q, k, k)
+    o2, l2 = impl.standard_attention(q, k, k)
+    if not (_close(o1, o2) and _close(l1, l2)):
+        fails.append("gqa with one query head per key/value head must be standard attention")
+    return fails
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_blockwise_equals_full,
@@ -258,6 +296,7 @@ ALL_CHECKS = [
     check_closed_forms,
     check_invariants,
     check_split_merge,
+    check_gqa,
 ]
 
 

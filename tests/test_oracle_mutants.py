@@ -93,6 +93,18 @@ def _merge_unweighted(ms, ls, os_):
     return o, float(ms.max() + math.log(ls.sum()))
 
 
+def _gqa_modulo_mapping(q, k, v, scale=None, causal=False, rows=None):
+    # planted mistake: query head i uses key/value head i % h_kv
+    h_q, h_kv = q.shape[1], k.shape[1]
+    outs, lses = [], []
+    for i in range(h_q):
+        o, l = oracle.standard_attention(q[:, i], k[:, i % h_kv], v[:, i % h_kv], scale=scale,
+                                         causal=causal, rows=rows)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs, axis=1), np.stack(lses, axis=1)
+
+
 def _split_kv_with(merge):
     def f(q, k, v, num_splits, scale=None):
         return merge(*oracle.split_partials(q, k, v, num_splits, scale=scale))
@@ -113,6 +125,7 @@ MUTANTS = {
     "default_scale_1_over_d": _with(standard_attention=_std_factory(
         default_scale=lambda d: 1.0 / d)),
     "merge_ignores_weights": _with(split_kv_attention=_split_kv_with(_merge_unweighted)),
+    "gqa_modulo_head_mapping": _with(gqa_attention=_gqa_modulo_mapping),
 }
 
 
