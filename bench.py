@@ -426,23 +426,30 @@ def run_kernel_case(args):
     import torch
 
     from exact_io_aware_attn_gb300 import _lib, build as build_mod, cost
-    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL, WORKLOADS, make_workload
+    from exact_io_aware_attn_gb300.inputs import (DECODE, EXTRA_WORKLOADS, GPT2_PREFILL,
+                                                  WORKLOADS, make_workload)
 
     build_mod.build()
-    named = {w.name: w for w in WORKLOADS}
+    named = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
     w = {"prefill": GPT2_PREFILL, "decode": DECODE}.get(args.kernel_case) or named[args.kernel_case]
     if args.case_batch:
         w = dataclasses.replace(w, B=args.case_batch)
     q, k, v = (t.cuda() for t in make_workload(w))
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if w.kv_heads != w.h:
+        def call():
+            _lib.attn_fwd_gqa(q, k, v, causal=w.causal, out=o, lse=lse)
+    else:
+        def call():
+            _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
     for _ in range(args.warmup):
-        _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+        call()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(args.steps):
-        _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+        call()
     b.record()
     torch.cuda.synchronize()
     st, word = _lib.get_device_error()
@@ -450,7 +457,7 @@ def run_kernel_case(args):
         raise SystemExit(f"device status {st} ({word:#x})")
     sec = a.elapsed_time(b) / max(1, args.steps) * 1e-3
     fl = cost.flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
-    by = cost.min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d)
+    by = cost.min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d, h_kv=w.kv_heads)
     peaks = load_peaks()
     print(json.dumps({"workload": w.name, "B": w.B, "kernel": _lib.last_kernel_name(),
                       "us_per_call": sec * 1e6, "tflops": fl / sec / 1e12,

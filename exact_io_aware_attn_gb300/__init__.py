@@ -11,6 +11,8 @@ from ._lib import (  # noqa: F401
     AttnError,
     abi_version,
     attn_fwd,
+    attn_fwd_decode_noalloc,
+    attn_fwd_gqa,
     decode_num_splits,
     fwd_raw,
     get_device_error,

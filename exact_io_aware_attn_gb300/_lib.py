@@ -38,6 +38,9 @@ SIGNATURES = {
     "attn_last_kernel_name": (ctypes.c_char_p, []),
     "attn_fwd_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_uint, _VP]),
+    "attn_fwd_gqa": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP,
+                          _SZ, _VP]),
+    "attn_gqa_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
 }
 
 # Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
@@ -98,6 +101,48 @@ def get_device_error(stream=None):
     word = ctypes.c_uint(0)
     st = lib().attn_get_device_error(_stream_ptr(stream), ctypes.byref(word))
     return int(st), int(word.value)
+
+
+def gqa_workspace_bytes(B, h_q, h_kv, T_q, T_kv, d, num_splits=0) -> int:
+    return int(lib().attn_gqa_workspace_bytes(B, h_q, h_kv, T_q, T_kv, d, num_splits))
+
+
+def fwd_gqa_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h_q, h_kv, T_q, T_kv, d, scale, causal,
+                dtype, num_splits=0, workspace_ptr=None, workspace_nbytes=0, stream_ptr=None) -> int:
+    """Direct call of attn_fwd_gqa; returns the status code."""
+    return int(lib().attn_fwd_gqa(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h_q, h_kv, T_q, T_kv, d,
+                                  float(scale), int(causal), int(dtype), int(num_splits),
+                                  workspace_ptr, int(workspace_nbytes), stream_ptr))
+
+
+def attn_fwd_gqa(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_splits=0,
+                 stream=None):
+    """Grouped-query attention: q [B, h_q, T_q, d]; k, v [B, h_kv, T_kv, d]
+    with h_q a multiple of h_kv. Returns (o like q, lse [B, h_q, T_q] fp32).
+    The decode workspace comes from the library's stream-ordered allocation."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, h_q, T_q, d = q.shape
+    h_kv, T_kv = k.shape[1], k.shape[2]
+    if k.shape != (B, h_kv, T_kv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, h_kv, T_kv, d]")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, h_q, T_q), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = fwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         B, h_q, h_kv, T_q, T_kv, d, scale, causal, _dtype_code(q), num_splits,
+                         None, 0, _stream_ptr(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_gqa")
+    return out, lse
 
 
 def selftest_wait_timeout(limit_us, stream=None) -> int:

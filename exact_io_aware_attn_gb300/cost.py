@@ -25,9 +25,10 @@ def flops(B: int, h: int, T_q: int, T_kv: int, d: int, causal: bool) -> int:
     return 4 * d * B * h * visible_pairs(T_q, T_kv, causal)
 
 
-def min_bytes(B: int, h: int, T_q: int, T_kv: int, d: int, elem: int = 2) -> int:
+def min_bytes(B: int, h: int, T_q: int, T_kv: int, d: int, elem: int = 2, h_kv: int = 0) -> int:
+    """h_kv: key/value heads under grouped-query attention (0 = h)."""
     qo = 2 * B * h * T_q * d * elem
-    kv = 2 * B * h * T_kv * d * elem
+    kv = 2 * B * (h_kv or h) * T_kv * d * elem
     lse = B * h * T_q * 4
     return qo + kv + lse
 

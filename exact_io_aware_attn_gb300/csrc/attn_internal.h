@@ -20,6 +20,7 @@ struct FwdProblem {
   int causal;
   int bf16;               // 1 = bf16, 0 = fp16
   unsigned int* status;   // device status word of the current device
+  int h_kv;               // key/value heads; h is a multiple of it (h_kv == h: plain attention)
 };
 
 // Prefill (T_q > 1): tcgen05 tensor-core kernel. `name` receives a static
@@ -31,16 +32,24 @@ cudaError_t launch_prefill(const FwdProblem& p, cudaStream_t stream, const char*
 cudaError_t launch_decode(const FwdProblem& p, int num_splits, float* ws, cudaStream_t stream,
                           const char** name);
 
+// Query heads one decode split CTA serves (all sharing one key/value head):
+// the largest of 8, 4, 2, 1 that divides the group size h / h_kv.
+inline int decode_heads_per_cta(int group) {
+  return (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : (group % 2 == 0) ? 2 : 1;
+}
+
 // Split kernel occupancy (CTAs per SM) for the split-count heuristic.
-int decode_split_ctas_per_sm(int d, int bf16);
+int decode_split_ctas_per_sm(int d, int heads_per_cta);
 
 namespace detail {
 // Argument checks shared by every entry point (attn_api.cu); *empty is set
 // when the output has no elements.
 attn_status_t validate(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
-             int T_q, int T_kv, int d, float scale, int causal, int dtype, bool* empty);
-// Decode split count chosen by shape on the current device (attn_api.cu).
-int choose_splits(int B, int h, int T_kv, int d, int bf16);
+                       int T_q, int T_kv, int d, float scale, int causal, int dtype, bool* empty,
+                       int h_kv = -1);
+// Decode split count chosen by shape on the current device (attn_api.cu):
+// `rows` CTAs per partition index (B * h_kv * group / heads_per_cta).
+int choose_splits(long long rows, int T_kv, int d, int heads_per_cta);
 }  // namespace detail
 
 // Floats per partial: d outputs, then running max and running sum, padded

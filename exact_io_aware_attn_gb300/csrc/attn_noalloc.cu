@@ -60,13 +60,14 @@ extern "C" attn_status_t attn_fwd_decode_noalloc(const void* q, const void* k, c
   if (num_splits < 0 || num_splits > 1024) return ATTN_ERR_INVALID_ARG;
   if (empty) return ATTN_OK;
   const int bf16 = dtype == ATTN_BF16 ? 1 : 0;
-  const int splits = num_splits > 0 ? num_splits : attn::detail::choose_splits(B, h, T_kv, d, 1);
+  const int splits =
+      num_splits > 0 ? num_splits : attn::detail::choose_splits(static_cast<long long>(B) * h, T_kv, d, 1);
   if (static_cast<long long>(B) * h * splits > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
   const size_t need = static_cast<size_t>(B) * h * splits * attn::decode_partial_floats(d);
   if (need > kScratchFloats) return ATTN_ERR_WORKSPACE;  // beyond the fixed scratch
   float* ws = scratch_ptr();
   if (!ws) return ATTN_ERR_CUDA;
-  attn::FwdProblem p{q, k, v, o, lse, B, h, 1, T_kv, d, scale, 0, bf16, nullptr};
+  attn::FwdProblem p{q, k, v, o, lse, B, h, 1, T_kv, d, scale, 0, bf16, nullptr, h};
   const char* name = nullptr;
   return attn::launch_decode(p, splits, ws, static_cast<cudaStream_t>(stream), &name) ==
                  cudaSuccess

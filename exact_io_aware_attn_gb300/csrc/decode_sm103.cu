@@ -88,11 +88,13 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[N], f
   m = mn;
 }
 
+// One CTA: partition s of the keys of one query head (one query head per
+// CTA: plain attention, or a grouped-query group of odd size).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kDecThreads)
-    decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,
-                        const uint8_t* __restrict__ v, float* __restrict__ ws, int T_kv, int S,
-                        int chunk, float scale_log2) {
+    decode_split_1head_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,
+                              const uint8_t* __restrict__ v, float* __restrict__ ws, int T_kv,
+                              int S, int chunk, float scale_log2, int group) {
   constexpr int TPK = D / 8;            // threads per key
   constexpr int KPW = 32 / TPK;         // keys per warp per load
   constexpr int SLOTS = (kDecThreads / 32) * KPW;
@@ -113,8 +115,11 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
   for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
 
-  const uint8_t* kp = k + static_cast<size_t>(bh) * T_kv * ROW + sub * 16;
-  const uint8_t* vp = v + static_cast<size_t>(bh) * T_kv * ROW + sub * 16;
+  // key/value head of this query head: with h_q = group * h_kv,
+  // (b * h_q + i) / group = b * h_kv + i / group (group = 1: plain attention)
+  const int kvbh = bh / group;
+  const uint8_t* kp = k + static_cast<size_t>(kvbh) * T_kv * ROW + sub * 16;
+  const uint8_t* vp = v + static_cast<size_t>(kvbh) * T_kv * ROW + sub * 16;
 
   float m = -INFINITY, l = 0.f;
   float o[8];
@@ -210,6 +215,164 @@ __global__ void __launch_bounds__(kDecThreads)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// One CTA: partition s of the keys of one key/value head, for G query heads
+// that share it (grouped-query attention; G = 1 for plain attention). Every
+// cached key and value row is read once and used for all G heads.
+template <int D, bool BF16, int G>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,
+                        const uint8_t* __restrict__ v, float* __restrict__ ws, int T_kv, int S,
+                        int chunk, float scale_log2, int h_q, int h_kv) {
+  constexpr int TPK = D / 8;            // threads per key
+  constexpr int KPW = 32 / TPK;         // keys per warp per load
+  constexpr int SLOTS = (kDecThreads / 32) * KPW;
+  constexpr int ROW = D * 2;            // bytes per key row
+  constexpr int UNR = (G >= 8) ? 1 : (G >= 4) ? 2 : kUnroll;  // keys in flight per thread
+
+  const int s = static_cast<int>(blockIdx.x % static_cast<unsigned>(S));
+  const int grp = static_cast<int>(blockIdx.x / static_cast<unsigned>(S));
+  const int group = h_q / h_kv;
+  const int n_sub = group / G;          // CTAs sharing one key/value head
+  const int kvbh = grp / n_sub;         // b * h_kv + key/value head
+  const int b = kvbh / h_kv;
+  const int hq0 = (kvbh % h_kv) * group + (grp % n_sub) * G;  // first query head
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % TPK;           // which 8 dims
+  const int slot = warp * KPW + lane / TPK;
+
+  const int lo = s * chunk;
+  const int hi = min(lo + chunk, T_kv);
+
+  float qf[G][8];
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    const size_t bhq = static_cast<size_t>(b) * h_q + hq0 + i;
+    unpack8<BF16>(*reinterpret_cast<const uint4*>(q + bhq * ROW + sub * 16), qf[i]);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) qf[i][t] *= scale_log2;
+  }
+
+  const uint8_t* kp = k + static_cast<size_t>(kvbh) * T_kv * ROW + sub * 16;
+  const uint8_t* vp = v + static_cast<size_t>(kvbh) * T_kv * ROW + sub * 16;
+
+  float m[G], l[G], o[G][8];
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) o[i][t] = 0.f;
+  }
+
+  for (int base = lo; base < hi; base += SLOTS * UNR) {
+    uint4 kr[UNR], vr[UNR];
+    bool valid[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int key = base + u * SLOTS + slot;
+      valid[u] = key < hi;
+      if (valid[u]) {
+        kr[u] = ld_stream(kp + static_cast<size_t>(key) * ROW);
+        vr[u] = ld_stream(vp + static_cast<size_t>(key) * ROW);
+      } else {
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float sc[UNR][G];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      float kf[8];
+      unpack8<BF16>(kr[u], kf);
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        float dot = 0.f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) dot = fmaf(qf[i][t], kf[t], dot);
+#pragma unroll
+        for (int w = 1; w < TPK; w <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
+        sc[u][i] = valid[u] ? dot : -INFINITY;
+      }
+    }
+    // unpack each value row once for all G heads
+    float vf[UNR][8];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) unpack8<BF16>(vr[u], vf[u]);
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      float mt = m[i];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) mt = fmaxf(mt, sc[u][i]);
+      const float ref = (mt == -INFINITY) ? 0.f : mt;
+      const float a = ex2f(m[i] - ref);
+      l[i] *= a;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) o[i][t] *= a;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const float pr = ex2f(sc[u][i] - ref);
+        l[i] += pr;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[i][t] = fmaf(pr, vf[u][t], o[i][t]);
+      }
+      m[i] = mt;
+    }
+  }
+
+  // Merge the key slots of this warp (lanes with the same `sub`), head by head.
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+#pragma unroll
+    for (int w = TPK; w < 32; w <<= 1) {
+      float o2[8];
+      const float m2 = __shfl_xor_sync(0xffffffffu, m[i], w);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l[i], w);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) o2[t] = __shfl_xor_sync(0xffffffffu, o[i][t], w);
+      merge_state<8>(m[i], l[i], o[i], m2, l2, o2);
+    }
+  }
+  // Then the four warps.
+  __shared__ float sh_o[4][G][D];
+  __shared__ float sh_ml[4][G][2];
+  if (lane < TPK) {
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) sh_o[warp][i][sub * 8 + t] = o[i][t];
+      if (lane == 0) {
+        sh_ml[warp][i][0] = m[i];
+        sh_ml[warp][i][1] = l[i];
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0 && lane < TPK) {
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+#pragma unroll
+      for (int w = 1; w < 4; ++w) {
+        float o2[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o2[t] = sh_o[w][i][sub * 8 + t];
+        merge_state<8>(m[i], l[i], o[i], sh_ml[w][i][0], sh_ml[w][i][1], o2);
+      }
+      const size_t bhq = static_cast<size_t>(b) * h_q + hq0 + i;
+      float* part = ws + (bhq * S + s) * decode_partial_floats(D);
+      *reinterpret_cast<float4*>(part + sub * 8) = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+      *reinterpret_cast<float4*>(part + sub * 8 + 4) =
+          make_float4(o[i][4], o[i][5], o[i][6], o[i][7]);
+      if (lane == 0) *reinterpret_cast<float4*>(part + D) = make_float4(m[i], l[i], 0.f, 0.f);
+    }
+  }
+  // The merge kernel is launched as a programmatic dependent of this grid:
+  // once every CTA has passed this point (or exited) it may be scheduled, and
+  // it waits (griddepcontrol.wait) for this grid's completion and memory
+  // flush before reading any partial.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128)
     decode_combine_kernel(const float* __restrict__ ws, uint8_t* __restrict__ out,
@@ -284,15 +447,22 @@ __global__ void __launch_bounds__(128)
   if (lane == 0) lse[bh] = (M + __log2f(L)) * 0.69314718055994531f;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, int G>
 cudaError_t launch_t(const FwdProblem& p, int S, float* ws, cudaStream_t stream) {
   const int BH = p.B * p.h;
+  const long long rows = static_cast<long long>(p.B) * p.h_kv * ((p.h / p.h_kv) / G);
   const int chunk = (p.T_kv + S - 1) / S;
   const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-  dim3 g1(static_cast<unsigned>(S) * static_cast<unsigned>(BH));
-  decode_split_kernel<D, BF16><<<g1, kDecThreads, 0, stream>>>(
-      static_cast<const uint8_t*>(p.q), static_cast<const uint8_t*>(p.k),
-      static_cast<const uint8_t*>(p.v), ws, p.T_kv, S, chunk, scale_log2);
+  dim3 g1(static_cast<unsigned>(S) * static_cast<unsigned>(rows));
+  if constexpr (G == 1) {
+    decode_split_1head_kernel<D, BF16><<<g1, kDecThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(p.q), static_cast<const uint8_t*>(p.k),
+        static_cast<const uint8_t*>(p.v), ws, p.T_kv, S, chunk, scale_log2, p.h / p.h_kv);
+  } else {
+    decode_split_kernel<D, BF16, G><<<g1, kDecThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(p.q), static_cast<const uint8_t*>(p.k),
+        static_cast<const uint8_t*>(p.v), ws, p.T_kv, S, chunk, scale_log2, p.h, p.h_kv);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the merge is a programmatic dependent launch: it may start while the
@@ -311,32 +481,60 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* ws, cudaStream_t stream)
                             static_cast<uint8_t*>(p.o), p.lse, BH, S);
 }
 
+template <int D, bool BF16>
+cudaError_t launch_g(const FwdProblem& p, int S, float* ws, cudaStream_t stream) {
+  switch (decode_heads_per_cta(p.h / p.h_kv)) {
+    case 8: return launch_t<D, BF16, 8>(p, S, ws, stream);
+    case 4: return launch_t<D, BF16, 4>(p, S, ws, stream);
+    case 2: return launch_t<D, BF16, 2>(p, S, ws, stream);
+    default: return launch_t<D, BF16, 1>(p, S, ws, stream);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const FwdProblem& p, int num_splits, float* ws, cudaStream_t stream,
                           const char** name) {
   cudaError_t e;
+  const bool gqa = p.h_kv != p.h;
   if (p.d == 64) {
-    e = p.bf16 ? launch_t<64, true>(p, num_splits, ws, stream)
-               : launch_t<64, false>(p, num_splits, ws, stream);
-    *name = p.bf16 ? "decode_split_d64_bf16+decode_combine" : "decode_split_d64_f16+decode_combine";
+    e = p.bf16 ? launch_g<64, true>(p, num_splits, ws, stream)
+               : launch_g<64, false>(p, num_splits, ws, stream);
+    *name = gqa ? (p.bf16 ? "decode_split_gqa_d64_bf16+decode_combine"
+                          : "decode_split_gqa_d64_f16+decode_combine")
+                : (p.bf16 ? "decode_split_d64_bf16+decode_combine"
+                          : "decode_split_d64_f16+decode_combine");
   } else {
-    e = p.bf16 ? launch_t<128, true>(p, num_splits, ws, stream)
-               : launch_t<128, false>(p, num_splits, ws, stream);
-    *name = p.bf16 ? "decode_split_d128_bf16+decode_combine" : "decode_split_d128_f16+decode_combine";
+    e = p.bf16 ? launch_g<128, true>(p, num_splits, ws, stream)
+               : launch_g<128, false>(p, num_splits, ws, stream);
+    *name = gqa ? (p.bf16 ? "decode_split_gqa_d128_bf16+decode_combine"
+                          : "decode_split_gqa_d128_f16+decode_combine")
+                : (p.bf16 ? "decode_split_d128_bf16+decode_combine"
+                          : "decode_split_d128_f16+decode_combine");
   }
   return e;
 }
 
-int decode_split_ctas_per_sm(int d, int bf16) {
+int decode_split_ctas_per_sm(int d, int heads_per_cta) {
   int n = 0;
-  cudaError_t e;
-  if (d == 64)
-    e = bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<64, true>, kDecThreads, 0)
-             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<64, false>, kDecThreads, 0);
-  else
-    e = bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<128, true>, kDecThreads, 0)
-             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<128, false>, kDecThreads, 0);
+  cudaError_t e = cudaErrorInvalidValue;
+  const size_t smem = 0;
+  auto occ = [&](auto kern) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecThreads, smem); };
+  if (d == 64) {
+    switch (heads_per_cta) {
+      case 8: e = occ(decode_split_kernel<64, true, 8>); break;
+      case 4: e = occ(decode_split_kernel<64, true, 4>); break;
+      case 2: e = occ(decode_split_kernel<64, true, 2>); break;
+      default: e = occ(decode_split_1head_kernel<64, true>); break;
+    }
+  } else {
+    switch (heads_per_cta) {
+      case 8: e = occ(decode_split_kernel<128, true, 8>); break;
+      case 4: e = occ(decode_split_kernel<128, true, 4>); break;
+      case 2: e = occ(decode_split_kernel<128, true, 2>); break;
+      default: e = occ(decode_split_1head_kernel<128, true>); break;
+    }
+  }
   return (e == cudaSuccess && n > 0) ? n : 8;
 }
 

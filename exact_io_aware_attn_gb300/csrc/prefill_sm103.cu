@@ -183,14 +183,16 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 // One work unit: query tiles A = rows [q0, q0+128) and B = [q0+128, q0+256)
 // of head bh, and how many key tiles each must see.
 struct Unit {
-  int bh, q0, rows_b, n_a, n_b, n_all;
+  int bh, kvbh, q0, rows_b, n_a, n_b, n_all;
 };
 
 __device__ __forceinline__ Unit unit_info(int u, int BH, int n_pairs, int T_q, int T_kv,
-                                          int causal) {
+                                          int causal, int h_q, int h_kv) {
   Unit w;
   const int pair = n_pairs - 1 - u / BH;  // heaviest pairs first under a causal mask
   w.bh = u % BH;
+  // grouped-query attention: query head i reads key/value head i / (h_q / h_kv)
+  w.kvbh = (w.bh / h_q) * h_kv + (w.bh % h_q) / (h_q / h_kv);
   w.q0 = pair * 2 * kBM;
   const int rows_a = min(kBM, T_q - w.q0);
   w.rows_b = max(0, min(kBM, T_q - w.q0 - kBM));
@@ -220,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, void* __restrict__ out,
                    float* __restrict__ lse, int T_q, int T_kv, int BH, int n_pairs,
-                   float scale_log2, int causal, unsigned int* __restrict__ status) {
+                   float scale_log2, int causal, unsigned int* __restrict__ status, int h_q,
+                   int h_kv) {
   using C = Cfg<D>;
   constexpr int SL = C::SLOTS;
   extern __shared__ uint8_t smem_raw[];
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
           ok = ptx::mbar_wait(q_empty, (nq & 1) ^ 1, status, status_word(kKernPrefill, kSiteProdQ));
           if (!ok) break;
           ptx::mbar_arrive_expect_tx(q_full, C::TILE_BYTES * (w.rows_b > 0 ? 2 : 1));
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
                 ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot], c * 64,
-                                 j * kBN, w.bh, pol_kv);
+                                 j * kBN, w.kvbh, pol_kv);
               ++g;
             }
           }
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
           ok = ptx::mbar_wait(q_full, nq & 1, status, status_word(kKernPrefill, kSiteMmaQ));
           ++nq;
           if (!ok) break;
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; ok && rr * G < U; ++rr) {
       const int u = unit_of_round(rr, bid, G);
       if (u >= U) continue;
-      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal);
+      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
       const int n_x = x ? w.n_b : w.n_a;
       if (n_x == 0) continue;
       const int row = w.q0 + x * kBM + r;        // absolute query row
@@ -653,8 +656,9 @@ cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
   }
   const int BH = p.B * p.h;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.T_q, BH, D, BF16) || !make_map(&mk, p.k, p.T_kv, BH, D, BF16) ||
-      !make_map(&mv, p.v, p.T_kv, BH, D, BF16))
+  const int BH_kv = p.B * p.h_kv;
+  if (!make_map(&mq, p.q, p.T_q, BH, D, BF16) || !make_map(&mk, p.k, p.T_kv, BH_kv, D, BF16) ||
+      !make_map(&mv, p.v, p.T_kv, BH_kv, D, BF16))
     return cudaErrorInvalidValue;
   const int n_qtiles = (p.T_q + kBM - 1) / kBM;
   const int n_pairs = (n_qtiles + 1) / 2;
@@ -663,7 +667,7 @@ cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
   const int grid = static_cast<int>(units < sms ? units : sms);
   const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p.o, p.lse, p.T_q, p.T_kv, BH, n_pairs,
-                                                  scale_log2, p.causal, p.status);
+                                                  scale_log2, p.causal, p.status, p.h, p.h_kv);
   return cudaGetLastError();
 }
 

@@ -39,6 +39,7 @@ class Workload:
     causal: bool
     mult: float = 1.0
     seed: int = 0
+    h_kv: int = 0        # key/value heads (grouped-query attention); 0 = h
 
     @property
     def torch_dtype(self):
@@ -52,8 +53,12 @@ class Workload:
     def scale(self) -> float:
         return self.d ** -0.5
 
+    @property
+    def kv_heads(self) -> int:
+        return self.h_kv or self.h
+
     def describe(self) -> dict:
-        return {"workload": self.name, "B": self.B, "h": self.h,
+        return {"workload": self.name, "B": self.B, "h": self.h, "h_kv": self.kv_heads,
                 "T_q": self.T_q, "T_kv": self.T_kv, "d": self.d,
                 "dtype": self.dtype_name, "causal": self.causal,
                 "input_scale": self.mult, "seed": self.seed}
@@ -70,9 +75,16 @@ DECODE = Workload("decode_B32_h12_Tkv16384_d64_bf16", 32, 12, 1, 16384, 64, BF16
 
 WORKLOADS = [TINY, GPT2_PREFILL, LONG_4K, LONG_8K, LONG_8K_D128, VERY_LONG, DECODE]
 
+# Grouped-query decode (a widening beyond the five workloads above): 32 query
+# heads share 8 key/value heads, the geometry of common grouped-query models.
+DECODE_GQA = Workload("decode_gqa_B32_hq32_hkv8_Tkv16384_d128_bf16", 32, 32, 1, 16384, 128, BF16,
+                      False, h_kv=8)
+EXTRA_WORKLOADS = [DECODE_GQA]
 
-def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu"):
-    """Draw q [B,h,T_q,d], k and v [B,h,T_kv,d] as 16-bit tensors.
+
+def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu", h_kv=None):
+    """Draw q [B,h,T_q,d], k and v [B,h_kv,T_kv,d] (h_kv defaults to h) as
+    16-bit tensors.
 
     The draw happens on the CPU generator (so every machine gets the same
     values) and the result is then moved to `device`.
@@ -80,8 +92,9 @@ def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu"):
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     out = []
-    for t in (T_q, T_kv, T_kv):
-        x = torch.randn((B, h, t, d), generator=gen, dtype=torch.float32)
+    hk = h if h_kv is None else h_kv
+    for heads, t in ((h, T_q), (hk, T_kv), (hk, T_kv)):
+        x = torch.randn((B, heads, t, d), generator=gen, dtype=torch.float32)
         if mult != 1.0:
             x.mul_(mult)
         out.append(x.to(_TORCH_DTYPE[dtype]).to(device))
@@ -89,4 +102,4 @@ def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu"):
 
 
 def make_workload(w: Workload, device="cpu"):
-    return make_qkv(w.B, w.h, w.T_q, w.T_kv, w.d, w.dtype, w.mult, w.seed, device)
+    return make_qkv(w.B, w.h, w.T_q, w.T_kv, w.d, w.dtype, w.mult, w.seed, device, w.kv_heads)

@@ -109,6 +109,32 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
                           void* stream);
 
 /*
+ * attn_fwd_gqa -- grouped-query attention: q and o have h_q heads, k and v
+ * have h_kv heads, h_q a multiple of h_kv; query head i attends with
+ * key/value head i / (h_q / h_kv) ("Attention and Its Computational Cost",
+ * section "The other shape": fewer key and value heads shrink the cache and
+ * its read per step). Layouts: q, o [B][h_q][T_q][d]; k, v [B][h_kv][T_kv][d];
+ * lse [B][h_q][T_q]. Other arguments as in attn_fwd_ex; with workspace NULL
+ * and workspace_bytes 0 the decode path takes its workspace from the
+ * stream-ordered allocator as attn_fwd does. The decode path reads each
+ * cached key/value row once for up to 8 query heads of its group.
+ * h_kv == h_q is plain attention (same kernels as attn_fwd_ex).
+ * Returns ATTN_ERR_INVALID_ARG if h_kv < 1 or h_q is not a multiple of h_kv.
+ */
+attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int h_q, int h_kv, int T_q, int T_kv, int d, float scale,
+                           int causal, int dtype, int num_splits, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * attn_gqa_workspace_bytes -- workspace attn_fwd_gqa needs (0 for the
+ * prefill path or invalid sizes): B*h_q*S*(d+4)*4 bytes, S the partition
+ * count (num_splits, or the library's choice for this grouping when 0).
+ */
+size_t attn_gqa_workspace_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int d,
+                                int num_splits);
+
+/*
  * attn_workspace_bytes -- bytes of workspace attn_fwd_ex needs for this
  * shape (0 for the prefill path). num_splits as in attn_fwd_ex (0 = the
  * library's choice). Returns 0 for invalid sizes. The decode workspace holds

@@ -83,6 +83,26 @@ def check_case(B, h, T_q, T_kv, d, dtype, causal, mult=1.0, seed=0, scale=None, 
                    absolute=mult <= 1.0)
 
 
+def gpu_fwd_gqa(q, k, v, causal, num_splits=0):
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=dev)
+    _lib.attn_fwd_gqa(qd, kd, vd, causal=causal, out=o, lse=lse, num_splits=num_splits)
+    torch.cuda.synchronize()
+    st, word = _lib.get_device_error()
+    assert st == _lib.ATTN_OK, f"device status {st} word {word:#x}"
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def oracle_fwd_gqa(q, k, v, causal, rows=None):
+    s = oracle_scale(q.shape[-1] ** -0.5)
+    qn, kn, vn = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    o_ref, lse_ref = oracle.gqa_attention(qn, kn, vn, scale=s, causal=causal, rows=rows)
+    o_abs, _ = oracle.gqa_attention(qn, kn, np.abs(vn), scale=s, causal=causal, rows=rows)
+    return o_ref, lse_ref, o_abs
+
+
 def sample_rows(T_q, n_random=12, seed=0):
     """Rows that exercise every kind of tile position: first/last rows of
     tiles, the ragged tail, and a few random ones."""

@@ -145,7 +145,7 @@ def test_auto_split_count_is_in_range(L):
     for (B, h, T) in ((32, 12, 16384), (1, 12, 16384), (1, 1, 100), (64, 12, 1024), (1, 1, 1)):
         s = _lib.decode_num_splits(B, h, T, 64)
         assert 1 <= s <= 1024
-        assert s == 1 or -(-T // s) >= 64       # at least 64 keys per partition
+        assert s == 1 or T // s >= 128          # at least 128 keys per partition
         assert _lib.workspace_bytes(B, h, 1, T, 64, 0) == B * h * s * 68 * 4
     assert _lib.decode_num_splits(0, 12, 100, 64) == 0
 
@@ -179,3 +179,33 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 def test_selftest_limit_validated_before_launch(L):
     assert _lib.selftest_wait_timeout(0) == _lib.ATTN_ERR_INVALID_ARG
     assert _lib.selftest_wait_timeout(2000001) == _lib.ATTN_ERR_INVALID_ARG
+
+
+def _gqa(**over):
+    a = dict(B=2, h_q=8, h_kv=2, T_q=1, T_kv=300, d=64, scale=0.125, causal=0,
+             dtype=_lib.ATTN_BF16, num_splits=0)
+    a.update(over)
+    return _lib.fwd_gqa_raw(Q, K, V, O, LSE, a["B"], a["h_q"], a["h_kv"], a["T_q"], a["T_kv"],
+                            a["d"], a["scale"], a["causal"], a["dtype"], a["num_splits"],
+                            a.get("ws"), a.get("nbytes", 0), None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(h_kv=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(h_kv=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(h_kv=3), _lib.ATTN_ERR_INVALID_ARG),          # 8 is not a multiple of 3
+    (dict(h_kv=16), _lib.ATTN_ERR_INVALID_ARG),         # more kv heads than query heads
+    (dict(d=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(num_splits=2000), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(ws=WS, nbytes=16), _lib.ATTN_ERR_WORKSPACE),  # caller workspace too small
+    (dict(B=0), _lib.ATTN_OK),                          # empty
+])
+def test_gqa_arguments(L, over, status):
+    assert _gqa(**over) == status
+
+
+def test_gqa_workspace_bytes(L):
+    assert _lib.gqa_workspace_bytes(2, 8, 2, 1, 300, 64, 16) == 2 * 8 * 16 * 68 * 4
+    assert _lib.gqa_workspace_bytes(2, 8, 2, 300, 300, 64, 16) == 0     # prefill
+    assert _lib.gqa_workspace_bytes(2, 8, 3, 1, 300, 64, 16) == 0       # invalid grouping
+    assert _lib.gqa_workspace_bytes(2, 8, 8, 1, 300, 64, 0) == _lib.workspace_bytes(2, 8, 1, 300, 64, 0)
