@@ -4,8 +4,10 @@ tests, the smoke check and the benchmark's CPU-baseline leg, never by the
 product path."""
 
 from .oracle import (  # noqa: F401
+    attention_backward,
     causal_visible,
     gqa_attention,
+    gqa_attention_backward,
     merge_partials,
     online_attention,
     online_softmax_states,

@@ -24,6 +24,12 @@ Pages followed (cited by page title and section):
   section "What is being computed": per head Q is T_q x d, K and V are
   T_kv x d, over B sequences and h heads; causal: position i sees keys up to
   and including itself.
+* Backward pass: "IO-Aware Attention: Tiling the Score Matrix Without
+  Materializing It", section "What has to stay in fast memory" says only that
+  the backward pass recomputes the softmax output from the saved Q, K, V and
+  the per-row constants. The gradients themselves are not printed; the
+  oracle takes the plainest reading, the derivative of the forward above
+  written out by the chain rule (attention_backward).
 
 Readings where the pages are silent (each is listed in the design doc):
 
@@ -56,6 +62,8 @@ __all__ = [
     "split_kv_attention",
     "causal_visible",
     "gqa_attention",
+    "attention_backward",
+    "gqa_attention_backward",
 ]
 
 
@@ -285,3 +293,92 @@ def gqa_attention(q, k, v, scale=None, causal=False, rows=None):
         outs.append(o)
         lses.append(l)
     return np.stack(outs, axis=1), np.stack(lses, axis=1)
+
+
+def attention_backward(q, k, v, do, scale=None, causal=False):
+    """Gradients of attention, float64: returns (dQ, dK, dV).
+
+    The derivative of O = softmax(scale * Q K^T [masked]) V with respect to
+    Q, K and V, given the incoming gradient dO (same shape as O), by the
+    chain rule through the materialised forward of standard_attention:
+
+        P   = softmax of the masked scaled scores, row by row
+        dV  = P^T dO
+        dP  = dO V^T
+        dS  = P * (dP - rowsum(P * dP))      (softmax Jacobian, row by row)
+        dQ  = scale * dS K
+        dK  = scale * dS^T Q
+
+    Masked entries have P = 0 and so dS = 0. The pages state that the
+    backward pass recomputes P from Q, K, V and the saved row constants
+    ("IO-Aware Attention: Tiling the Score Matrix Without Materializing It",
+    section "What has to stay in fast memory") but print no gradient
+    formulas; these are the calculus of the forward definition.
+
+    Shapes: q [..., T_q, d], k and v [..., T_kv, d], do [..., T_q, d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    if q.ndim < 2 or k.ndim != q.ndim or v.ndim != q.ndim or do.shape[:-1] != q.shape[:-1]:
+        raise ValueError("q, k, v, do must have the same rank >= 2 and do the rows of q")
+    t_q, d = q.shape[-2], q.shape[-1]
+    t_kv = k.shape[-2]
+    if k.shape[-1] != d or v.shape[-2] != t_kv or do.shape[-1] != v.shape[-1]:
+        raise ValueError("shape mismatch between q, k, v and do")
+    if t_kv < 1:
+        raise ValueError("softmax over zero keys is undefined")
+    if causal and t_q > t_kv:
+        raise ValueError("causal attention needs T_q <= T_kv")
+    if scale is None:
+        scale = _default_scale(d)
+    lead = q.shape[:-2]
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    visible = causal_visible(t_q, t_kv) if causal else None
+    for idx in np.ndindex(*lead):
+        s = scale * (q[idx] @ k[idx].T)
+        if causal:
+            s = np.where(visible, s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        p = e / e.sum(axis=1, keepdims=True)
+        dv[idx] = p.T @ do[idx]
+        dp = do[idx] @ v[idx].T
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        dq[idx] = scale * (ds @ k[idx])
+        dk[idx] = scale * (ds.T @ q[idx])
+    return dq, dk, dv
+
+
+def gqa_attention_backward(q, k, v, do, scale=None, causal=False):
+    """Gradients of grouped-query attention, float64: returns (dQ, dK, dV).
+
+    q, do: [B, h_q, T_q, d]; k, v: [B, h_kv, T_kv, d]. Query head i reads
+    key/value head i // (h_q // h_kv) (gqa_attention), so a key/value head's
+    gradient is the sum of the gradients its query heads send it; each query
+    head's own gradients are attention_backward against that head.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4 or do.shape != q.shape:
+        raise ValueError("q, do must be [B, h_q, T_q, d] and k, v [B, h_kv, T_kv, d]")
+    h_q, h_kv = q.shape[1], k.shape[1]
+    if h_kv < 1 or h_q % h_kv != 0:
+        raise ValueError("h_q must be a positive multiple of h_kv")
+    group = h_q // h_kv
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for i in range(h_q):
+        j = i // group
+        dqi, dki, dvi = attention_backward(q[:, i], k[:, j], v[:, j], do[:, i], scale=scale,
+                                           causal=causal)
+        dq[:, i] = dqi
+        dk[:, j] += dki
+        dv[:, j] += dvi
+    return dq, dk, dv

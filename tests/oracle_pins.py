@@ -12,7 +12,12 @@ The checks draw on:
 * invariants (key shift, joint key/value permutation, affine maps of V,
   folding a factor of q into the scale),
 * exactness of the blocking and of the split merge (block sizes 1..n,
-  partition counts 1..n+3).
+  partition counts 1..n+3),
+* for the gradients: the library's autograd through float64
+  scaled_dot_product_attention, central finite differences of the
+  pure-Python brute force, closed forms (one key, equal value rows, causal
+  row 0) and invariants (sum over keys of dK is zero, key shift, scale
+  folding, linearity in dO).
 """
 
 from __future__ import annotations
@@ -38,6 +43,8 @@ def real_oracle():
         merge_partials=oracle.merge_partials,
         split_kv_attention=oracle.split_kv_attention,
         gqa_attention=oracle.gqa_attention,
+        attention_backward=oracle.attention_backward,
+        gqa_attention_backward=oracle.gqa_attention_backward,
     )
 
 
@@ -288,6 +295,168 @@ def check_gqa(impl):
     return fails
 
 
+def _autograd_sdpa(q, k, v, do, causal, scale=None, gqa=False):
+    """Gradients from the library: torch autograd through float64 SDPA."""
+    import torch
+    import torch.nn.functional as F
+    tq, tk, tv = (torch.from_numpy(np.array(x)).requires_grad_(True) for x in (q, k, v))
+    t_q, t_kv = q.shape[-2], k.shape[-2]
+    mask = (torch.ones(t_q, t_kv, dtype=torch.bool).tril(diagonal=t_kv - t_q)
+            if causal else None)
+    o = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale, enable_gqa=gqa)
+    o.backward(torch.from_numpy(np.array(do)))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def check_backward_library(impl):
+    fails = []
+    rng = _rng(8)
+    for (b, h, t_q, t_kv, d) in ((1, 2, 16, 16, 8), (2, 1, 5, 19, 16), (1, 3, 1, 40, 8),
+                                 (1, 1, 7, 7, 4)):
+        q = rng.standard_normal((b, h, t_q, d))
+        k = rng.standard_normal((b, h, t_kv, d))
+        v = rng.standard_normal((b, h, t_kv, d))
+        do = rng.standard_normal((b, h, t_q, d))
+        for causal in (False, True):
+            for scale in (None, 0.3):
+                ref = _autograd_sdpa(q, k, v, do, causal, scale)
+                got = impl.attention_backward(q, k, v, do, scale=scale, causal=causal)
+                for name, a, r in zip(("dq", "dk", "dv"), got, ref):
+                    if not _close(a, r, rtol=1e-9, atol=1e-11):
+                        fails.append(f"{name} vs library autograd shape={(b, h, t_q, t_kv, d)} "
+                                     f"causal={causal} scale={scale}")
+    return fails
+
+
+def check_backward_finite_difference(impl):
+    """Central differences of L = sum(O * dO), O from the pure-Python brute
+    force, against the oracle's gradients on tiny inputs."""
+    fails = []
+    rng = _rng(9)
+    eps = 1e-6
+    for t_q, t_kv, d, causal in ((3, 4, 3, False), (3, 4, 3, True), (4, 4, 2, True)):
+        q = rng.standard_normal((t_q, d))
+        k = rng.standard_normal((t_kv, d))
+        v = rng.standard_normal((t_kv, d))
+        do = rng.standard_normal((t_q, d))
+        scale = 0.6
+        got = impl.attention_backward(q, k, v, do, scale=scale, causal=causal)
+
+        def loss(qq, kk, vv):
+            o, _ = _brute(qq.tolist(), kk.tolist(), vv.tolist(), scale, causal)
+            return math.fsum((o * do).ravel().tolist())
+
+        for which, (name, g) in enumerate(zip(("dq", "dk", "dv"), got)):
+            x = [q, k, v][which]
+            num = np.empty_like(x)
+            for idx in np.ndindex(*x.shape):
+                args_p = [q.copy(), k.copy(), v.copy()]
+                args_m = [q.copy(), k.copy(), v.copy()]
+                args_p[which][idx] += eps
+                args_m[which][idx] -= eps
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            if not _close(g, num, rtol=1e-6, atol=1e-7):
+                fails.append(f"{name} vs finite differences t_q={t_q} t_kv={t_kv} causal={causal}")
+    return fails
+
+
+def check_backward_closed_forms(impl):
+    fails = []
+    rng = _rng(10)
+    d = 5
+    # one key: P = 1 whatever the scores, so dQ = dK = 0 and dV = sum of dO
+    q = rng.standard_normal((4, d))
+    k1 = rng.standard_normal((1, d))
+    v1 = rng.standard_normal((1, d))
+    do = rng.standard_normal((4, d))
+    dq, dk, dv = impl.attention_backward(q, k1, v1, do, scale=0.5)
+    if not (_close(dq, 0 * dq) and _close(dk, 0 * dk) and _close(dv[0], do.sum(axis=0))):
+        fails.append("T_kv = 1 gradients")
+    # equal value rows: O = v whatever P is, so dQ = dK = 0; dV = P^T dO
+    # still sums to the sum of dO over the keys (columns of P^T sum to 1)
+    k6 = rng.standard_normal((6, d))
+    v6 = np.repeat(rng.standard_normal((1, d)), 6, axis=0)
+    for causal in (False, True):
+        dq, dk, dv = impl.attention_backward(q, k6, v6, do, scale=0.5, causal=causal)
+        if not (_close(dq, 0 * dq, atol=1e-12) and _close(dk, 0 * dk, atol=1e-12)
+                and _close(dv.sum(axis=0), do.sum(axis=0))):
+            fails.append(f"equal value rows gradients (causal={causal})")
+    # causal, square: row 0 sees only key 0, so dQ[0] = 0 and dO[0] flows
+    # into dV[0] alone
+    q5 = rng.standard_normal((5, d))
+    k5 = rng.standard_normal((5, d))
+    v5 = rng.standard_normal((5, d))
+    do5 = np.zeros((5, d))
+    do5[0] = rng.standard_normal(d)
+    dq, dk, dv = impl.attention_backward(q5, k5, v5, do5, scale=0.3, causal=True)
+    if not (_close(dq[0], 0 * dq[0]) and _close(dv[0], do5[0]) and _close(dv[1:], 0 * dv[1:])
+            and _close(dk, 0 * dk)):
+        fails.append("causal row 0 gradients")
+    # dO = 0: every gradient is 0
+    dq, dk, dv = impl.attention_backward(q5, k5, v5, np.zeros((5, d)), causal=True)
+    if not (_close(dq, 0 * dq) and _close(dk, 0 * dk) and _close(dv, 0 * dv)):
+        fails.append("zero incoming gradient")
+    return fails
+
+
+def check_backward_invariants(impl):
+    fails = []
+    rng = _rng(11)
+    t_q, t_kv, d = 6, 9, 4
+    q = rng.standard_normal((t_q, d))
+    k = rng.standard_normal((t_kv, d))
+    v = rng.standard_normal((t_kv, d))
+    do = rng.standard_normal((t_q, d))
+    s = 0.45
+    for causal in (False, True):
+        dq, dk, dv = impl.attention_backward(q, k, v, do, scale=s, causal=causal)
+        # rows of dS sum to zero, so the key gradients sum to zero
+        if not _close(dk.sum(axis=0), np.zeros(d), atol=1e-12):
+            fails.append(f"sum of dK over keys must vanish (causal={causal})")
+        # a shift of every key leaves P, and so every gradient, unchanged
+        u = rng.standard_normal(d)
+        g2 = impl.attention_backward(q, k + u, v, do, scale=s, causal=causal)
+        if not all(_close(a, b, rtol=1e-9, atol=1e-11) for a, b in zip(g2, (dq, dk, dv))):
+            fails.append(f"key shift invariance of the gradients (causal={causal})")
+        # folding a factor into q: dQ scales by 1/a, dK and dV do not change
+        a = 2.5
+        g3 = impl.attention_backward(a * q, k, v, do, scale=s / a, causal=causal)
+        if not (_close(g3[0], dq / a, rtol=1e-9, atol=1e-11)
+                and _close(g3[1], dk, rtol=1e-9, atol=1e-11) and _close(g3[2], dv)):
+            fails.append(f"scale folding of the gradients (causal={causal})")
+        # gradients are linear in dO
+        g4 = impl.attention_backward(q, k, v, -3.0 * do, scale=s, causal=causal)
+        if not all(_close(x4, -3.0 * x, rtol=1e-10, atol=1e-12) for x4, x in zip(g4, (dq, dk, dv))):
+            fails.append(f"linearity in dO (causal={causal})")
+    return fails
+
+
+def check_backward_gqa(impl):
+    fails = []
+    rng = _rng(12)
+    for (b, h_q, h_kv, t_q, t_kv, d) in ((2, 4, 2, 5, 9, 8), (1, 6, 3, 7, 7, 4)):
+        q = rng.standard_normal((b, h_q, t_q, d))
+        k = rng.standard_normal((b, h_kv, t_kv, d))
+        v = rng.standard_normal((b, h_kv, t_kv, d))
+        do = rng.standard_normal((b, h_q, t_q, d))
+        for causal in (False, True):
+            ref = _autograd_sdpa(q, k, v, do, causal, gqa=True)
+            got = impl.gqa_attention_backward(q, k, v, do, causal=causal)
+            for name, a, r in zip(("dq", "dk", "dv"), got, ref):
+                if not _close(a, r, rtol=1e-9, atol=1e-11):
+                    fails.append(f"gqa {name} vs library autograd shape={(b, h_q, h_kv)} "
+                                 f"causal={causal}")
+    q = rng.standard_normal((1, 3, 4, 8))
+    k = rng.standard_normal((1, 3, 6, 8))
+    v = rng.standard_normal((1, 3, 6, 8))
+    do = rng.standard_normal((1, 3, 4, 8))
+    g1 = impl.gqa_attention_backward(q, k, v, do)
+    g2 = impl.attention_backward(q, k, v, do)
+    if not all(_close(a, b) for a, b in zip(g1, g2)):
+        fails.append("gqa backward with one query head per key/value head")
+    return fails
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_blockwise_equals_full,
@@ -297,6 +466,11 @@ ALL_CHECKS = [
     check_invariants,
     check_split_merge,
     check_gqa,
+    check_backward_library,
+    check_backward_finite_difference,
+    check_backward_closed_forms,
+    check_backward_invariants,
+    check_backward_gqa,
 ]
 
 

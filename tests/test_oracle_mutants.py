@@ -111,6 +111,46 @@ def _split_kv_with(merge):
     return f
 
 
+def _bwd_factory(drop_d=False, dk_from_ds=False, dq_scale=True, dv_unnormalised=False,
+                 causal_off=0):
+    def bwd(q, k, v, do, scale=None, causal=False):
+        q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+        t_q, t_kv, d = q.shape[-2], k.shape[-2], q.shape[-1]
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+        for idx in np.ndindex(*q.shape[:-2]):
+            s_ = scale * (q[idx] @ k[idx].T)
+            if causal:
+                vis = np.arange(t_kv)[None, :] <= np.arange(t_q)[:, None] + (t_kv - t_q) + causal_off
+                s_ = np.where(vis, s_, -np.inf)
+            e = np.exp(s_ - s_.max(axis=1, keepdims=True))
+            p = e / e.sum(axis=1, keepdims=True)
+            dv[idx] = (e if dv_unnormalised else p).T @ do[idx]
+            dp = do[idx] @ v[idx].T
+            ds = p * dp if drop_d else p * (dp - (p * dp).sum(axis=1, keepdims=True))
+            dq[idx] = (scale if dq_scale else 1.0) * (ds @ k[idx])
+            # planted: dS (not its transpose) against Q, padded to the key count
+            dk[idx] = scale * (ds.T @ q[idx] if not dk_from_ds else
+                               np.resize(ds @ q[idx] if t_q == t_kv else ds.T @ q[idx][::-1],
+                                         (t_kv, d)))
+        return dq, dk, dv
+    return bwd
+
+
+def _gqa_bwd_overwrites(q, k, v, do, scale=None, causal=False):
+    # planted mistake: each query head overwrites its key/value head's
+    # gradient instead of adding to it
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    group = q.shape[1] // k.shape[1]
+    dq, dk, dv = np.empty_like(q), np.zeros_like(k), np.zeros_like(v)
+    for i in range(q.shape[1]):
+        j = i // group
+        dq[:, i], dk[:, j], dv[:, j] = oracle.attention_backward(q[:, i], k[:, j], v[:, j], do[:, i],
+                                                                 scale=scale, causal=causal)
+    return dq, dk, dv
+
+
 MUTANTS = {
     "online_drops_rescale": _with(online_attention=_online_factory(rescale=False)),
     "online_rescale_wrong_sign": _with(online_attention=_online_factory(sign=-1.0)),
@@ -126,6 +166,12 @@ MUTANTS = {
         default_scale=lambda d: 1.0 / d)),
     "merge_ignores_weights": _with(split_kv_attention=_split_kv_with(_merge_unweighted)),
     "gqa_modulo_head_mapping": _with(gqa_attention=_gqa_modulo_mapping),
+    "backward_drops_row_term": _with(attention_backward=_bwd_factory(drop_d=True)),
+    "backward_dk_untransposed": _with(attention_backward=_bwd_factory(dk_from_ds=True)),
+    "backward_dq_missing_scale": _with(attention_backward=_bwd_factory(dq_scale=False)),
+    "backward_dv_unnormalised_p": _with(attention_backward=_bwd_factory(dv_unnormalised=True)),
+    "backward_causal_excludes_diagonal": _with(attention_backward=_bwd_factory(causal_off=-1)),
+    "gqa_backward_overwrites": _with(gqa_attention_backward=_gqa_bwd_overwrites),
 }
 
 
