@@ -443,6 +443,17 @@ def run_kernel_case(args):
     else:
         def call():
             _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+    if args.backward:
+        from exact_io_aware_attn_gb300.inputs import make_dout
+        call()
+        dout = make_dout(w.B, w.h, w.T_q, w.d, w.dtype, w.seed, device=q.device)
+        grads = [torch.empty_like(t) for t in (q, k, v)]
+        ws = torch.empty(_lib.bwd_workspace_bytes(w.B, w.h, w.T_q, w.T_kv, w.d), dtype=torch.uint8,
+                         device=q.device)
+
+        def call():
+            _lib.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, dq=grads[0], dk=grads[1],
+                          dv=grads[2], workspace=ws)
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
@@ -456,10 +467,15 @@ def run_kernel_case(args):
     if st != _lib.ATTN_OK:
         raise SystemExit(f"device status {st} ({word:#x})")
     sec = a.elapsed_time(b) / max(1, args.steps) * 1e-3
-    fl = cost.flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
-    by = cost.min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d, h_kv=w.kv_heads)
+    if args.backward:
+        fl = cost.bwd_flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
+        by = cost.bwd_min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d, h_kv=w.kv_heads)
+    else:
+        fl = cost.flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
+        by = cost.min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d, h_kv=w.kv_heads)
     peaks = load_peaks()
-    print(json.dumps({"workload": w.name, "B": w.B, "kernel": _lib.last_kernel_name(),
+    print(json.dumps({"workload": w.name, "pass": "backward" if args.backward else "forward",
+                      "B": w.B, "kernel": _lib.last_kernel_name(),
                       "us_per_call": sec * 1e6, "tflops": fl / sec / 1e12,
                       "gbs": by / sec / 1e9,
                       "frac_tensor_peak": fl / sec / 1e12 / peaks["bf16_tflops"],
@@ -478,6 +494,8 @@ def main(argv=None):
                     help="profiling mode: run only this call of the step, or a named workload")
     ap.add_argument("--case-batch", type=int, default=None,
                     help="batch size override for --kernel-case")
+    ap.add_argument("--backward", action="store_true",
+                    help="with --kernel-case: time the backward pass (attn_bwd) instead")
     args = ap.parse_args(argv)
     if args.kernel_case:
         return run_kernel_case(args)

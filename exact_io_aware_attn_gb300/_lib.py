@@ -1,7 +1,7 @@
 """ctypes binding of libattn.so (the C ABI declared in include/attn.h).
 
-Argument marshalling only: every step of the attention forward runs in the
-library's CUDA kernels. torch supplies device memory and the current
+Argument marshalling only: every step of the attention forward and backward
+runs in the library's CUDA kernels. torch supplies device memory and the current
 stream. There is no fallback: if the library is missing or a call fails,
 an exception says so.
 """
@@ -41,6 +41,11 @@ SIGNATURES = {
     "attn_fwd_gqa": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP,
                           _SZ, _VP]),
     "attn_gqa_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "attn_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I,
+                      _VP, _SZ, _VP]),
+    "attn_bwd_gqa": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F,
+                          _I, _I, _VP, _SZ, _VP]),
+    "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
 }
 
 # Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
@@ -272,3 +277,62 @@ def attn_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_split
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
     return out, lse
+
+
+def bwd_workspace_bytes(B, h, T_q, T_kv, d) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, h, T_q, T_kv, d))
+
+
+def bwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, B, h_q, h_kv,
+            T_q, T_kv, d, scale, causal, dtype, workspace_ptr=None, workspace_nbytes=0,
+            stream_ptr=None) -> int:
+    """Direct call of attn_bwd (h_kv == h_q) or attn_bwd_gqa; returns the
+    status code."""
+    L = lib()
+    if h_kv == h_q:
+        return int(L.attn_bwd(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr,
+                              B, h_q, T_q, T_kv, d, float(scale), int(causal), int(dtype),
+                              workspace_ptr, int(workspace_nbytes), stream_ptr))
+    return int(L.attn_bwd_gqa(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr,
+                              B, h_q, h_kv, T_q, T_kv, d, float(scale), int(causal), int(dtype),
+                              workspace_ptr, int(workspace_nbytes), stream_ptr))
+
+
+def attn_bwd(q, k, v, o, lse, dout, *, scale=None, causal=False, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attention from the forward's o and lse and
+    dout = dL/dO. q, o, dout: [B, h_q, T_q, d]; k, v: [B, h_kv, T_kv, d]
+    (h_kv < h_q: grouped-query attention); lse: fp32 [B, h_q, T_q] from the
+    forward with the same scale and causal flag. The workspace is taken
+    stream-ordered by the library unless given. Asynchronous."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise TypeError("q, k, v, o and dout must share one dtype")
+    B, h_q, T_q, d = q.shape
+    h_kv, T_kv = k.shape[1], k.shape[2]
+    if k.shape != (B, h_kv, T_kv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, h_kv, T_kv, d]")
+    if o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("o and dout must be shaped like q")
+    if lse.shape != (B, h_q, T_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, h_q, T_q] tensor")
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor like its input")
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with torch.cuda.device(q.device):
+        st = bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                     lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, h_q, h_kv,
+                     T_q, T_kv, d, scale, causal, _dtype_code(q), wp, wn, _stream_ptr(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv

@@ -25,7 +25,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 
-SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "attn_noalloc.cu"]
+SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "backward_sm103.cu",
+           "attn_noalloc.cu", "tma_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

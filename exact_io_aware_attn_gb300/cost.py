@@ -8,6 +8,13 @@ rows against T_kv keys, the keys j <= i + T_kv - T_q.
 Bytes: what the method must move at minimum -- Q, K, V read once, O written
 once (16-bit) and the fp32 logsumexp written once. The score and
 probability matrices are not counted: they never leave the chip.
+
+Backward: the gradient products dV = P^T dO, dP = dO V^T, dQ = dS K and
+dK = dS^T Q, plus recomputing S = Q K^T, are five products of 2*d FLOPs per
+visible pair: 10*d per pair per head (2.5x the forward). Recomputing S a
+second time, as a kernel that forms dQ apart from dK and dV does, is not
+counted. Minimum bytes: Q, K, V, O, dO and lse read once, dQ, dK, dV written
+once.
 """
 
 from __future__ import annotations
@@ -36,3 +43,13 @@ def min_bytes(B: int, h: int, T_q: int, T_kv: int, d: int, elem: int = 2, h_kv: 
 def kv_cache_bytes(B: int, h: int, T_kv: int, d: int, elem: int = 2) -> int:
     """The bytes a decode step must stream: every cached key and value."""
     return 2 * B * h * T_kv * d * elem
+
+
+def bwd_flops(B: int, h: int, T_q: int, T_kv: int, d: int, causal: bool) -> int:
+    return 10 * d * B * h * visible_pairs(T_q, T_kv, causal)
+
+
+def bwd_min_bytes(B: int, h: int, T_q: int, T_kv: int, d: int, elem: int = 2, h_kv: int = 0) -> int:
+    q_side = 4 * B * h * T_q * d * elem            # q, o, dO read; dQ written
+    kv_side = 4 * B * (h_kv or h) * T_kv * d * elem  # k, v read; dK, dV written
+    return q_side + kv_side + B * h * T_q * 4       # lse read

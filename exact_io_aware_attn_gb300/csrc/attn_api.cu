@@ -1,7 +1,8 @@
 // attn_api.cu -- the C ABI of libattn (declared in include/attn.h): argument
-// validation, prefill/decode dispatch, decode split choice, stream-ordered
-// workspace and the device status word. All compute happens in the kernels
-// of prefill_sm103.cu and decode_sm103.cu; nothing here computes attention.
+// validation, prefill/decode/backward dispatch, decode split choice,
+// stream-ordered workspace and the device status word. All compute happens
+// in the kernels of prefill_sm103.cu, decode_sm103.cu and backward_sm103.cu;
+// nothing here computes attention.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -234,6 +235,69 @@ attn_status_t run(const void* q, const void* k, const void* v, void* o, float* l
   return ATTN_OK;
 }
 
+// Backward: the forward's checks on (q, k, v, o, lse), then dout, the three
+// gradients and the workspace.
+attn_status_t run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int h, int h_kv,
+                      int T_q, int T_kv, int d, float scale, int causal, int dtype,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  bool empty = false;
+  attn_status_t st = validate(q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, h, T_q,
+                              T_kv, d, scale, causal, dtype, &empty, h_kv);
+  if (st != ATTN_OK) return st;
+  if (empty) {
+    t_last_kernel = "none";
+    return ATTN_OK;
+  }
+  const long long BH = static_cast<long long>(B) * h;
+  const long long key_tiles = (static_cast<long long>(T_kv) + 127) / 128;
+  const long long q_tiles = (static_cast<long long>(T_q) + 127) / 128;
+  // grids: one CTA per (key tile, kv head), one per (query tile, head), and
+  // the row-term pass at 16 rows per CTA over 128 rows per query tile
+  if (key_tiles * B * h_kv > 0x7fffffffll || q_tiles * BH * 8 > 0x7fffffffll)
+    return ATTN_ERR_UNSUPPORTED;
+  if (!dout || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qo_bytes = static_cast<size_t>(BH) * T_q * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(B) * h_kv * T_kv * d * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * T_q * 4;
+  struct Buf { const void* p; size_t n; };
+  const Buf ins[] = {{q, qo_bytes}, {k, kv_bytes}, {v, kv_bytes}, {o, qo_bytes},
+                     {dout, qo_bytes}, {lse, lse_bytes}};
+  const Buf outs[] = {{dq, qo_bytes}, {dk, kv_bytes}, {dv, kv_bytes}};
+  for (int i = 0; i < 3; ++i) {
+    for (const Buf& b : ins)
+      if (overlaps(outs[i].p, outs[i].n, b.p, b.n)) return ATTN_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return ATTN_ERR_INVALID_ARG;
+  }
+  const size_t need = attn::bwd_workspace_floats(BH, T_q) * sizeof(float);
+  const bool own = workspace == nullptr && workspace_bytes == 0;
+  if (!own) {
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ATTN_ERR_WORKSPACE;
+    for (const Buf& b : ins)
+      if (overlaps(workspace, need, b.p, b.n)) return ATTN_ERR_WORKSPACE;
+    for (const Buf& b : outs)
+      if (overlaps(workspace, need, b.p, b.n)) return ATTN_ERR_WORKSPACE;
+  }
+  attn::BwdProblem p{q, k, v, o, dout, lse, dq, dk, dv, B, h, h_kv, T_q, T_kv, d, scale, causal,
+                     dtype == ATTN_BF16 ? 1 : 0, nullptr, status_ptr()};
+  if (!p.status) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  if (own) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), need, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  p.ws = ws;
+  const char* name = "none";
+  const cudaError_t e = attn::launch_backward(p, s, &name);
+  if (own) cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  t_last_kernel = name;
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -278,6 +342,29 @@ size_t attn_workspace_bytes(int B, int h, int T_q, int T_kv, int d, int num_spli
   if (T_q != 1 || B == 0 || h == 0 || T_kv < 1) return 0;
   const int splits = num_splits > 0 ? num_splits : auto_splits(B, h, h, T_kv, d);
   return ws_bytes(B, h, d, splits);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int h, int T_q, int T_kv, int d, float scale, int causal, int dtype,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, h, h, T_q, T_kv, d, scale, causal, dtype,
+                 workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           int B, int h_q, int h_kv, int T_q, int T_kv, int d, float scale,
+                           int causal, int dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (h_kv < 1) return ATTN_ERR_INVALID_ARG;
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, h_q, h_kv, T_q, T_kv, d, scale, causal,
+                 dtype, workspace, workspace_bytes, stream);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int h, int T_q, int T_kv, int d) {
+  if (B < 1 || h < 1 || T_q < 1 || T_kv < 1 || (d != 64 && d != 128)) return 0;
+  return attn::bwd_workspace_floats(static_cast<long long>(B) * h, T_q) * sizeof(float);
 }
 
 int attn_decode_num_splits(int B, int h, int T_kv, int d) {

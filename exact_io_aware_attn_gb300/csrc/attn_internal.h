@@ -32,6 +32,35 @@ cudaError_t launch_prefill(const FwdProblem& p, cudaStream_t stream, const char*
 cudaError_t launch_decode(const FwdProblem& p, int num_splits, float* ws, cudaStream_t stream,
                           const char** name);
 
+// Backward pass (attn_bwd): gradients dq [B,h,T_q,d], dk and dv
+// [B,h_kv,T_kv,d] from q, k, v, the forward's o and lse, and dout = dO.
+struct BwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, h, h_kv, T_q, T_kv, d;
+  float scale;
+  int causal;
+  int bf16;
+  float* ws;              // bwd_workspace_floats(B*h, T_q) floats, 16-byte aligned
+  unsigned int* status;
+};
+
+// Query rows per head in the backward workspace: T_q rounded up to 128.
+inline size_t bwd_rows_padded(int T_q) { return (static_cast<size_t>(T_q) + 127) / 128 * 128; }
+// Two fp32 values (lse * log2 e and rowsum(dO * O)) per padded query row.
+inline size_t bwd_workspace_floats(long long BH, int T_q) {
+  return 2 * static_cast<size_t>(BH) * bwd_rows_padded(T_q);
+}
+
+cudaError_t launch_backward(const BwdProblem& p, cudaStream_t stream, const char** name);
+
 // Query heads one decode split CTA serves (all sharing one key/value head):
 // the largest of 8, 4, 2, 1 that divides the group size h / h_kv.
 inline int decode_heads_per_cta(int group) {

@@ -19,7 +19,10 @@ constexpr uint64_t kWaitLimitNs = 2000ull * 1000ull * 1000ull;
 
 constexpr uint32_t kStatusTimeout = 4u;  // == ATTN_ERR_TIMEOUT
 
-enum KernelId : uint32_t { kKernPrefill = 1, kKernDecodeSplit = 2, kKernDecodeCombine = 3, kKernSelftest = 4 };
+enum KernelId : uint32_t {
+  kKernPrefill = 1, kKernDecodeSplit = 2, kKernDecodeCombine = 3, kKernSelftest = 4,
+  kKernBwdKV = 5, kKernBwdQ = 6
+};
 
 __host__ __device__ constexpr uint32_t status_word(uint32_t kernel, uint32_t site) {
   return kStatusTimeout | (kernel << 8) | (site << 16);

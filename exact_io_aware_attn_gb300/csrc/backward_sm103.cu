@@ -1,0 +1,625 @@
+// backward_sm103.cu -- gradients of exact attention (dQ, dK, dV) on GB300
+// tensor cores, by recomputation.
+//
+// The backward pass does not keep the probabilities: it recomputes them from
+// Q, K, V and the per-row constants the forward saved (lse), one tile at a
+// time, and never writes a score or probability matrix to HBM ("IO-Aware
+// Attention: Tiling the Score Matrix Without Materializing It", section "What
+// has to stay in fast memory"). The gradients are the derivative of the
+// forward definition: with P = exp(scale * Q K^T - lse) (masked entries 0),
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  D_i = rowsum(dO_i * O_i),
+//   dQ = scale * dS K,  dK = scale * dS^T Q
+// (D_i = sum_j P_ij dP_ij because O_i = sum_j P_ij V_j).
+//
+// Three launches, no atomics (so the result is deterministic):
+//   bwd_prep     one pass over O and dO: D and lse * log2(e) per query row,
+//                into a workspace padded to 128 rows per head
+//   bwd (KV)     one CTA per (key/value head, 128-key tile): K and V stay in
+//                shared memory, the CTA streams 64-row tiles of Q and dO
+//                (every query head of the group, causal: only rows that see
+//                the tile) and accumulates dV and dK in tensor memory
+//   bwd (Q)      one CTA per (query head, 128-row tile): Q and dO stay, the
+//                CTA streams 64-key tiles of K and V (causal: up to the
+//                diagonal) and accumulates dQ in tensor memory
+//
+// Both modes are one kernel template. Roles (192 threads): warps 0-3 own
+// TMEM lanes 0-127 (one resident row each) and turn scores into P and dS;
+// warp 4 is the TMA producer; warp 5 owns TMEM and issues the MMAs. Per
+// streamed tile t the tensor core computes
+//   S_t  = X U_t^T and dP_t = Y W_t^T      (M=128 resident rows, N=64, K=d)
+// into one of two TMEM buffers, the elementwise warps store P_t and dS_t as
+// 16-bit over the first 32 columns of S_t and dP_t, and the tensor core then
+// accumulates (A read from TMEM, B the streamed tile read MN-major)
+//   KV mode (X=K, Y=V, U=Q, W=dO):  dV += P_t^T dO_t,  dK += dS_t^T Q_t
+//   Q mode  (X=Q, Y=dO, U=K, W=V):  dQ += dS_t K_t
+// The scores of tile t+1 go into the other buffer while the elementwise warps
+// work on tile t. TMEM: buffers [0,128) and [128,256) (S then dP, 64 columns
+// each), dV at 256, dK or dQ at 256 + d: 512 columns at d = 128.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "attn_status.h"
+#include "ptx_sm103.cuh"
+#include "tma_host.h"
+
+namespace attn {
+
+namespace {
+
+constexpr int kRes = 128;              // resident rows per CTA (TMEM lanes, M of every MMA)
+constexpr int kStr = 64;               // rows of one streamed tile
+constexpr int kSubRes = kRes * 128;    // one [128 rows][64 x 16-bit] swizzled sub-tile
+constexpr int kSubStr = kStr * 128;    // one [64 rows][64 x 16-bit] swizzled sub-tile
+constexpr int kBwdThreads = 192;
+constexpr int kWarpProd = 4;
+constexpr int kWarpMma = 5;
+constexpr uint32_t kColAcc1 = 256;     // dV (KV mode)
+
+template <int D, bool KV>
+struct BwdCfg {
+  static constexpr int RES_BYTES = kRes * D * 2;           // X or Y
+  static constexpr int STR_BYTES = kStr * D * 2;           // U or W
+  static constexpr int VEC_BYTES = KV ? 2 * kStr * 4 : 0;  // lse*log2e and D of the streamed rows
+  static constexpr int STAGE_BYTES = (2 * STR_BYTES + VEC_BYTES + 1023) / 1024 * 1024;
+  static constexpr int STAGES = (D == 64) ? 6 : 4;
+  static constexpr int OFF_X = 0;
+  static constexpr int OFF_Y = RES_BYTES;
+  static constexpr int OFF_RING = 2 * RES_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + STAGES * STAGE_BYTES;
+  // res_full, stage_full[ST], stage_empty[ST], sp_full[2], p_full[2], acc_full, mma_done
+  static constexpr int N_BARS = 1 + 2 * STAGES + 6;
+  static constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_ACC2 = 256u + D;             // dK (KV mode) or dQ (Q mode)
+};
+static_assert(BwdCfg<128, true>::SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(BwdCfg<128, false>::SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(BwdCfg<128, true>::COL_ACC2 + 128 <= 512, "tensor memory");
+
+__host__ __device__ constexpr uint32_t col_buf(int b) { return static_cast<uint32_t>(b) * 128u; }
+
+enum : uint32_t {
+  kSiteProdStage = 1, kSiteMmaRes, kSiteMmaStage, kSiteMmaP, kSiteEltS, kSiteEltStage, kSiteEltAcc
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+}
+
+__device__ __forceinline__ void tmem_wait_ld_64(uint32_t (&r)[64]) {
+#define R8(b) "+r"(r[b]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), "+r"(r[b + 4]), \
+              "+r"(r[b + 5]), "+r"(r[b + 6]), "+r"(r[b + 7])
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : R8(0), R8(8), R8(16), R8(24), R8(32), R8(40), R8(48), R8(56)
+               :
+               : "memory");
+#undef R8
+}
+
+__device__ __forceinline__ void tmem_wait_ld_32(uint32_t (&r)[32]) {
+#define R8(b) "+r"(r[b]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), "+r"(r[b + 4]), \
+              "+r"(r[b + 5]), "+r"(r[b + 6]), "+r"(r[b + 7])
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : R8(0), R8(8), R8(16), R8(24) : : "memory");
+#undef R8
+}
+
+// Bounded wait used only while draining after an error.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = ptx::smem_u32(bar);
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(a, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// D_i = sum_c dO_ic O_ic and lse_i * log2(e), per query row, into [BH][Tq_pad]
+// arrays; rows T_q..Tq_pad-1 of each head get D = 0 and +inf (so that any
+// probability recomputed for them is exactly 0).
+// ---------------------------------------------------------------------------
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    bwd_prep_kernel(const uint8_t* __restrict__ o, const uint8_t* __restrict__ dout,
+                    const float* __restrict__ lse, float* __restrict__ l2, float* __restrict__ dd,
+                    int T_q, int Tq_pad, long long n_rows) {
+  constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
+  const long long row = static_cast<long long>(blockIdx.x) * (256 / TPR) + threadIdx.x / TPR;
+  const int sub = threadIdx.x % TPR;
+  const bool in = row < n_rows;
+  const long long bh = in ? row / Tq_pad : 0;
+  const int t = in ? static_cast<int>(row - bh * Tq_pad) : 0;
+  const bool valid = in && t < T_q;
+  float acc = 0.f;
+  if (valid) {
+    const size_t e = (static_cast<size_t>(bh) * T_q + t) * D + sub * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + e * 2);
+    const uint4 g = *reinterpret_cast<const uint4*>(dout + e * 2);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = unpack2<BF16>(aw[i]), y = unpack2<BF16>(gw[i]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int w = 1; w < TPR; w <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+  if (in && sub == 0) {
+    dd[row] = valid ? acc : 0.f;
+    l2[row] = valid ? lse[static_cast<size_t>(bh) * T_q + t] * 1.4426950408889634f : INFINITY;
+  }
+}
+
+// One work unit: 128 resident rows of one head and the streamed tiles it
+// visits.
+struct BwdUnit {
+  int res_bh;    // KV: b * h_kv + key/value head; Q: b * h + query head
+  int r0;        // first resident row (key in KV mode, query row in Q mode)
+  int str_bh0;   // KV: first query head of the group; Q: the key/value head
+  int t_first;   // KV: first streamed 64-row tile of each query head; Q: 0
+  int per_head;  // streamed tiles per query head (KV) or in all (Q)
+  int n_items;
+};
+
+// Units are numbered heaviest first under a causal mask: key tile 0 is seen
+// by every query row, the last query tile sees the most keys.
+template <bool KV>
+__device__ __forceinline__ BwdUnit bwd_unit(int u, int BH_res, int n_res_tiles, int T_q, int T_kv,
+                                            int causal, int h, int h_kv) {
+  const int group = h / h_kv;
+  const int off = T_kv - T_q;
+  BwdUnit w;
+  w.res_bh = u % BH_res;
+  if constexpr (KV) {
+    const int j = u / BH_res;
+    w.r0 = j * kRes;
+    const int b = w.res_bh / h_kv, kvh = w.res_bh % h_kv;
+    w.str_bh0 = b * h + kvh * group;
+    // key r0 is visible to query row r iff r0 <= r + off
+    const int first_row = causal ? max(0, w.r0 - off) : 0;
+    w.t_first = first_row / kStr;
+    w.per_head = (T_q + kStr - 1) / kStr - w.t_first;
+    w.n_items = w.per_head * group;
+  } else {
+    const int i = n_res_tiles - 1 - u / BH_res;
+    w.r0 = i * kRes;
+    w.str_bh0 = w.res_bh / group;  // (b * h + i) / group = b * h_kv + i / group
+    w.t_first = 0;
+    const int last_row = min(T_q, w.r0 + kRes) - 1;
+    const int last_key = causal ? min(T_kv - 1, last_row + off) : T_kv - 1;
+    w.per_head = last_key / kStr + 1;
+    w.n_items = w.per_head;
+  }
+  return w;
+}
+
+__device__ __forceinline__ void bwd_item(const BwdUnit& w, int it, int* bh, int* s0) {
+  const int g = it / w.per_head;
+  *bh = w.str_bh0 + g;
+  *s0 = (w.t_first + (it - g * w.per_head)) * kStr;
+}
+
+template <int D, bool BF16, bool KV>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+               const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW,
+               const float* __restrict__ ws_l2, const float* __restrict__ ws_dd, int Tq_pad,
+               void* __restrict__ out1, void* __restrict__ out2, int T_q, int T_kv, int BH_res,
+               int n_res_tiles, int h, int h_kv, float scale, float scale_log2, int causal,
+               unsigned int* __restrict__ status) {
+  using C = BwdCfg<D, KV>;
+  constexpr int ST = C::STAGES;
+  constexpr uint32_t kKern = KV ? kKernBwdKV : kKernBwdQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* stage_full = bars + 1;
+  uint64_t* stage_empty = stage_full + ST;
+  uint64_t* sp_full = stage_empty + ST;
+  uint64_t* p_full = sp_full + 2;
+  uint64_t* acc_full = p_full + 2;
+  uint64_t* mma_done = acc_full + 1;
+  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMPTR);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const BwdUnit w =
+      bwd_unit<KV>(static_cast<int>(blockIdx.x), BH_res, n_res_tiles, T_q, T_kv, causal, h, h_kv);
+  const int n = w.n_items;
+  const int off = T_kv - T_q;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(res_full, 1);
+    for (int i = 0; i < ST; ++i) {
+      ptx::mbar_init(&stage_full[i], 1);
+      ptx::mbar_init(&stage_empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sp_full[b], 1);
+      ptx::mbar_init(&p_full[b], 128);
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(mma_done, 1);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == kWarpMma) {
+    ptx::tmem_alloc(tmem_ptr, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == kWarpProd) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmX);
+      ptx::prefetch_tensormap(&tmY);
+      ptx::prefetch_tensormap(&tmU);
+      ptx::prefetch_tensormap(&tmW);
+      // the streamed tiles are read by many CTAs (every key tile of a head,
+      // or every query tile): keep them in L2; the resident ones once
+      const uint64_t pol_str = ptx::policy_evict_last();
+      const uint64_t pol_res = ptx::policy_evict_first();
+      ptx::mbar_arrive_expect_tx(res_full, 2 * C::RES_BYTES);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        ptx::tma_load_3d(smem + C::OFF_X + c * kSubRes, &tmX, res_full, c * 64, w.r0, w.res_bh,
+                         pol_res);
+        ptx::tma_load_3d(smem + C::OFF_Y + c * kSubRes, &tmY, res_full, c * 64, w.r0, w.res_bh,
+                         pol_res);
+      }
+      bool ok = true;
+      int it = 0;
+      for (; it < n; ++it) {
+        const int slot = it % ST;
+        ok = ptx::mbar_wait(&stage_empty[slot], ((it / ST) & 1) ^ 1, status,
+                            status_word(kKern, kSiteProdStage));
+        if (!ok) break;
+        int sbh, s0;
+        bwd_item(w, it, &sbh, &s0);
+        uint8_t* stg = smem + C::OFF_RING + slot * C::STAGE_BYTES;
+        ptx::mbar_arrive_expect_tx(&stage_full[slot], 2 * C::STR_BYTES + C::VEC_BYTES);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          ptx::tma_load_3d(stg + c * kSubStr, &tmU, &stage_full[slot], c * 64, s0, sbh, pol_str);
+          ptx::tma_load_3d(stg + C::STR_BYTES + c * kSubStr, &tmW, &stage_full[slot], c * 64, s0,
+                           sbh, pol_str);
+        }
+        if constexpr (KV) {
+          const size_t vo = static_cast<size_t>(sbh) * Tq_pad + s0;
+          ptx::bulk_load(stg + 2 * C::STR_BYTES, ws_l2 + vo, kStr * 4, &stage_full[slot]);
+          ptx::bulk_load(stg + 2 * C::STR_BYTES + kStr * 4, ws_dd + vo, kStr * 4,
+                         &stage_full[slot]);
+        }
+      }
+      if (!ok) {
+        // let the copies in flight land before the CTA's shared memory goes
+        mbar_drain(res_full, 0);
+        for (int i = (it > ST ? it - ST : 0); i < it; ++i) mbar_drain(&stage_full[i % ST], (i / ST) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kRes, kStr, false, false);
+      constexpr uint32_t idG = ptx::make_idesc_f16(BF16, kRes, D, false, true);
+      const uint32_t sX = ptx::smem_u32(smem + C::OFF_X);
+      const uint32_t sY = ptx::smem_u32(smem + C::OFF_Y);
+      const uint32_t sR = ptx::smem_u32(smem + C::OFF_RING);
+      // K-major views (score products) and MN-major views (gradient products)
+      const uint64_t dX = ptx::make_sdesc_sw128(sX, 16, 1024);
+      const uint64_t dY = ptx::make_sdesc_sw128(sY, 16, 1024);
+      const uint64_t dUk = ptx::make_sdesc_sw128(sR, 16, 1024);
+      const uint64_t dWk = ptx::make_sdesc_sw128(sR + C::STR_BYTES, 16, 1024);
+      const uint64_t dUm = ptx::make_sdesc_sw128(sR, kSubStr, 1024);
+      const uint64_t dWm = ptx::make_sdesc_sw128(sR + C::STR_BYTES, kSubStr, 1024);
+
+      auto issue_scores = [&](int b, int slot) {
+        const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
+        const uint32_t d_s = tmem + col_buf(b);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ro = (kk >> 2) * kSubRes + (kk & 3) * 32;
+          const uint32_t to = (kk >> 2) * kSubStr + (kk & 3) * 32;
+          ptx::mma_f16_ss(d_s, dX + (ro >> 4), dUk + so + (to >> 4), idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ro = (kk >> 2) * kSubRes + (kk & 3) * 32;
+          const uint32_t to = (kk >> 2) * kSubStr + (kk & 3) * 32;
+          ptx::mma_f16_ss(d_s + 64, dY + (ro >> 4), dWk + so + (to >> 4), idS, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&sp_full[b]);
+      };
+      auto issue_grads = [&](int b, int slot, bool first) {
+        const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
+#pragma unroll
+        for (int kk = 0; kk < kStr / 16; ++kk) {
+          const uint64_t bo = static_cast<uint64_t>(kk * 16 * 128) >> 4;  // 16 streamed rows
+          const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
+          if constexpr (KV)
+            ptx::mma_f16_ts(tmem + kColAcc1, tmem + col_buf(b) + kk * 8, dWm + so + bo, idG, acc);
+          ptx::mma_f16_ts(tmem + C::COL_ACC2, tmem + col_buf(b) + 64 + kk * 8, dUm + so + bo, idG,
+                          acc);
+        }
+        ptx::mma_commit(&stage_empty[slot]);
+      };
+
+      bool ok = ptx::mbar_wait(res_full, 0, status, status_word(kKern, kSiteMmaRes));
+      if (ok)
+        ok = ptx::mbar_wait(&stage_full[0], 0, status, status_word(kKern, kSiteMmaStage));
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_scores(0, 0);
+      }
+      for (int it = 0; ok && it < n; ++it) {
+        const int b = it & 1;
+        if (it + 1 < n) {
+          // scores of the next tile into the other buffer: its previous
+          // contents (tile it-1) were read by tile it-1's gradient products,
+          // issued earlier by this thread and so executed earlier
+          const int s1 = (it + 1) % ST;
+          ok = ptx::mbar_wait(&stage_full[s1], ((it + 1) / ST) & 1, status,
+                              status_word(kKern, kSiteMmaStage));
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_scores(b ^ 1, s1);
+        }
+        ok = ptx::mbar_wait(&p_full[b], (it >> 1) & 1, status, status_word(kKern, kSiteMmaP));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_grads(b, it % ST, it == 0);
+      }
+      if (ok) ptx::mma_commit(acc_full);
+      // every MMA this thread issued must be complete before TMEM is freed
+      ptx::mma_commit(mma_done);
+      mbar_drain(mma_done, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    const int row = warp * 32 + lane;                  // TMEM lane = resident row
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int rrow = w.r0 + row;                       // KV: key index; Q: query row
+    float l2_row = 0.f, dd_row = 0.f;
+    if constexpr (!KV) {
+      const size_t ro = static_cast<size_t>(w.res_bh) * Tq_pad + rrow;  // rrow < Tq_pad
+      l2_row = ws_l2[ro];
+      dd_row = ws_dd[ro];
+    }
+    bool ok = true;
+    for (int it = 0; ok && it < n; ++it) {
+      const int b = it & 1;
+      const int slot = it % ST;
+      ok = ptx::mbar_wait(&sp_full[b], (it >> 1) & 1, status, status_word(kKern, kSiteEltS));
+      if constexpr (KV) {
+        // the row vectors arrived with the tile (TMA writes are visible to
+        // the threads that observe the stage barrier)
+        if (ok)
+          ok = ptx::mbar_wait(&stage_full[slot], (it / ST) & 1, status,
+                              status_word(kKern, kSiteEltStage));
+      }
+      // tcgen05.ld/st/wait are warp-collective: the whole warp takes every
+      // branch around them
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t sr[64], pr[64];
+      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b) + 64, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b) + 96, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+      tmem_wait_ld_64(sr);
+      tmem_wait_ld_64(pr);
+      const float* s = reinterpret_cast<const float*>(sr);
+      const float* dp = reinterpret_cast<const float*>(pr);
+
+      int sbh, s0;
+      bwd_item(w, it, &sbh, &s0);
+      // columns [cmin, cmax] of this row are visible
+      int cmin, cmax;
+      if constexpr (KV) {
+        cmin = causal ? rrow - off - s0 : INT_MIN / 2;   // query s0+c sees key rrow iff c >= cmin
+        cmax = kStr - 1;
+        if (rrow >= T_kv) cmin = kStr;                   // key past the end: nothing visible
+      } else {
+        cmin = 0;
+        cmax = (causal ? min(rrow + off, T_kv - 1) : T_kv - 1) - s0;
+      }
+      const bool all_visible = __all_sync(0xffffffffu, cmin <= 0 && cmax >= kStr - 1);
+      const float* vl2 = nullptr;
+      const float* vdd = nullptr;
+      if constexpr (KV) {
+        vl2 = reinterpret_cast<const float*>(smem + C::OFF_RING + slot * C::STAGE_BYTES +
+                                             2 * C::STR_BYTES);
+        vdd = vl2 + kStr;
+      }
+      uint32_t pk[32], gk[32];
+#pragma unroll
+      for (int c = 0; c < kStr; c += 2) {
+        float la, lb, da, db;
+        if constexpr (KV) {
+          const float2 l = *reinterpret_cast<const float2*>(vl2 + c);
+          const float2 dv = *reinterpret_cast<const float2*>(vdd + c);
+          la = l.x;
+          lb = l.y;
+          da = dv.x;
+          db = dv.y;
+        } else {
+          la = lb = l2_row;
+          da = db = dd_row;
+        }
+        float pa = ptx::ex2_approx(fmaf(s[c], scale_log2, -la));
+        float pb = ptx::ex2_approx(fmaf(s[c + 1], scale_log2, -lb));
+        if (!all_visible) {
+          pa = (c >= cmin && c <= cmax) ? pa : 0.f;
+          pb = (c + 1 >= cmin && c + 1 <= cmax) ? pb : 0.f;
+        }
+        pk[c >> 1] = pack2<BF16>(pa, pb);
+        gk[c >> 1] = pack2<BF16>(pa * (dp[c] - da), pb * (dp[c + 1] - db));
+      }
+      // P over the first 32 columns of S, dS over the first 32 of dP
+      ptx::tmem_st_32x32b_x32(t_lane + col_buf(b), pk);
+      ptx::tmem_st_32x32b_x32(t_lane + col_buf(b) + 64, gk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&p_full[b]);
+    }
+    if (ok) {
+      // -------------------------------------------------------------- epilogue
+      ok = ptx::mbar_wait(acc_full, 0, status, status_word(kKern, kSiteEltAcc));
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        ptx::tc_fence_after();
+        const int T_out = KV ? T_kv : T_q;
+        const bool write = rrow < T_out;
+#pragma unroll
+        for (int a = KV ? 0 : 1; a < 2; ++a) {
+          uint8_t* dst = reinterpret_cast<uint8_t*>(a == 0 ? out1 : out2) +
+                         (static_cast<size_t>(w.res_bh) * T_out + (write ? rrow : 0)) * D * 2;
+          const float mul = a == 0 ? 1.f : scale;
+          const uint32_t col = a == 0 ? kColAcc1 : C::COL_ACC2;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t raw[32];
+            ptx::tmem_ld_32x32b_x32(t_lane + col + c * 32, raw);
+            tmem_wait_ld_32(raw);
+            if (write) {
+#pragma unroll
+              for (int g8 = 0; g8 < 4; ++g8) {
+                const float* f = reinterpret_cast<const float*>(&raw[g8 * 8]);
+                uint4 v;
+                v.x = pack2<BF16>(f[0] * mul, f[1] * mul);
+                v.y = pack2<BF16>(f[2] * mul, f[3] * mul);
+                v.z = pack2<BF16>(f[4] * mul, f[5] * mul);
+                v.w = pack2<BF16>(f[6] * mul, f[7] * mul);
+                *reinterpret_cast<uint4*>(dst + (c * 32 + g8 * 8) * 2) = v;
+              }
+            }
+          }
+        }
+      }
+    }
+    ptx::tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == kWarpMma) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <typename K>
+cudaError_t configure_once(K kern, int smem_bytes, uint64_t* configured, int dev) {
+  if (dev >= 64 || (*configured & (1ull << dev))) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess) *configured |= 1ull << dev;
+  return e;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_t(const BwdProblem& p, cudaStream_t stream) {
+  using CK = BwdCfg<D, true>;
+  using CQ = BwdCfg<D, false>;
+  auto kern_kv = bwd_kernel<D, BF16, true>;
+  auto kern_q = bwd_kernel<D, BF16, false>;
+  static std::mutex mu;
+  static uint64_t conf_kv = 0, conf_q = 0;  // one bit per device ordinal
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    e = configure_once(kern_kv, CK::SMEM_BYTES, &conf_kv, dev);
+    if (e == cudaSuccess) e = configure_once(kern_q, CQ::SMEM_BYTES, &conf_q, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const int BH = p.B * p.h;
+  const int BH_kv = p.B * p.h_kv;
+  const int Tq_pad = static_cast<int>(bwd_rows_padded(p.T_q));
+  float* l2 = p.ws;
+  float* dd = p.ws + static_cast<size_t>(BH) * Tq_pad;
+  const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+
+  // 1. row terms
+  const long long n_rows = static_cast<long long>(BH) * Tq_pad;
+  const long long rpb = 256 / (D / 8);
+  bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((n_rows + rpb - 1) / rpb), 256, 0, stream>>>(
+      static_cast<const uint8_t*>(p.o), static_cast<const uint8_t*>(p.dout), p.lse, l2, dd, p.T_q,
+      Tq_pad, n_rows);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  // 2. dK, dV: resident K/V tiles, streamed Q/dO tiles
+  CUtensorMap mX, mY, mU, mW;
+  if (!make_map(&mX, p.k, p.T_kv, BH_kv, D, BF16, kRes) ||
+      !make_map(&mY, p.v, p.T_kv, BH_kv, D, BF16, kRes) ||
+      !make_map(&mU, p.q, p.T_q, BH, D, BF16, kStr) ||
+      !make_map(&mW, p.dout, p.T_q, BH, D, BF16, kStr))
+    return cudaErrorInvalidValue;
+  const int n_kt = (p.T_kv + kRes - 1) / kRes;
+  kern_kv<<<static_cast<unsigned>(BH_kv) * n_kt, kBwdThreads, CK::SMEM_BYTES, stream>>>(
+      mX, mY, mU, mW, l2, dd, Tq_pad, p.dv, p.dk, p.T_q, p.T_kv, BH_kv, n_kt, p.h, p.h_kv, p.scale,
+      scale_log2, p.causal, p.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  // 3. dQ: resident Q/dO tiles, streamed K/V tiles
+  if (!make_map(&mX, p.q, p.T_q, BH, D, BF16, kRes) ||
+      !make_map(&mY, p.dout, p.T_q, BH, D, BF16, kRes) ||
+      !make_map(&mU, p.k, p.T_kv, BH_kv, D, BF16, kStr) ||
+      !make_map(&mW, p.v, p.T_kv, BH_kv, D, BF16, kStr))
+    return cudaErrorInvalidValue;
+  const int n_qt = (p.T_q + kRes - 1) / kRes;
+  kern_q<<<static_cast<unsigned>(BH) * n_qt, kBwdThreads, CQ::SMEM_BYTES, stream>>>(
+      mX, mY, mU, mW, l2, dd, Tq_pad, nullptr, p.dq, p.T_q, p.T_kv, BH, n_qt, p.h, p.h_kv, p.scale,
+      scale_log2, p.causal, p.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdProblem& p, cudaStream_t stream, const char** name) {
+  cudaError_t e;
+  if (p.d == 64) {
+    e = p.bf16 ? launch_bwd_t<64, true>(p, stream) : launch_bwd_t<64, false>(p, stream);
+    *name = p.bf16 ? "bwd_prep+bwd_dkdv+bwd_dq_tcgen05_d64_bf16"
+                   : "bwd_prep+bwd_dkdv+bwd_dq_tcgen05_d64_f16";
+  } else {
+    e = p.bf16 ? launch_bwd_t<128, true>(p, stream) : launch_bwd_t<128, false>(p, stream);
+    *name = p.bf16 ? "bwd_prep+bwd_dkdv+bwd_dq_tcgen05_d128_bf16"
+                   : "bwd_prep+bwd_dkdv+bwd_dq_tcgen05_d128_f16";
+  }
+  return e;
+}
+
+}  // namespace attn

@@ -51,6 +51,7 @@
 
 #include "attn_internal.h"
 #include "ptx_sm103.cuh"
+#include "tma_host.h"
 
 namespace attn {
 
@@ -588,55 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<EncodeTiledFn>(nullptr);
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
-// [BH][T][D] 16-bit tensor viewed as 3-D (D innermost), box 64 x 128 x 1,
-// 128-byte swizzle; rows past T read as zero.
-bool make_map(CUtensorMap* map, const void* base, int T, int BH, int D, bool bf16) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(T) * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                   const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-int device_sms(int dev) {
-  static std::mutex mu;
-  static int sms[64] = {};
-  if (dev < 0 || dev >= 64) return 148;
-  std::lock_guard<std::mutex> g(mu);
-  if (!sms[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    sms[dev] = n;
-  }
-  return sms[dev];
-}
-
 template <int D, bool BF16>
 cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
   using C = Cfg<D>;
@@ -657,8 +609,9 @@ cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
   const int BH = p.B * p.h;
   CUtensorMap mq, mk, mv;
   const int BH_kv = p.B * p.h_kv;
-  if (!make_map(&mq, p.q, p.T_q, BH, D, BF16) || !make_map(&mk, p.k, p.T_kv, BH_kv, D, BF16) ||
-      !make_map(&mv, p.v, p.T_kv, BH_kv, D, BF16))
+  if (!make_map(&mq, p.q, p.T_q, BH, D, BF16, kBM) ||
+      !make_map(&mk, p.k, p.T_kv, BH_kv, D, BF16, kBN) ||
+      !make_map(&mv, p.v, p.T_kv, BH_kv, D, BF16, kBN))
     return cudaErrorInvalidValue;
   const int n_qtiles = (p.T_q + kBM - 1) / kBM;
   const int n_pairs = (n_qtiles + 1) / 2;

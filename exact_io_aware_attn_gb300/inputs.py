@@ -103,3 +103,14 @@ def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu", h_k
 
 def make_workload(w: Workload, device="cpu"):
     return make_qkv(w.B, w.h, w.T_q, w.T_kv, w.d, w.dtype, w.mult, w.seed, device, w.kv_heads)
+
+
+def make_dout(B, h, T_q, d, dtype=BF16, seed=0, device="cpu"):
+    """The incoming gradient dO [B, h, T_q, d] for backward tests and
+    benchmarks: N(0,1) in float32 from its own seeded CPU generator (seed +
+    1000003, so it is independent of q, k, v drawn with `seed`), cast to the
+    16-bit dtype."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed + 1000003)
+    x = torch.randn((B, h, T_q, d), generator=gen, dtype=torch.float32)
+    return x.to(_TORCH_DTYPE[dtype]).to(device)

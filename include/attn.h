@@ -1,5 +1,6 @@
 /*
- * attn.h -- C ABI of libattn: exact IO-aware attention forward on GB300.
+ * attn.h -- C ABI of libattn: exact IO-aware attention on GB300, forward and
+ * backward.
  *
  * What it computes (per batch element b and head h):
  *
@@ -60,7 +61,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 typedef enum {
   ATTN_OK = 0,
@@ -181,11 +182,64 @@ int attn_abi_version(void);
 
 /*
  * attn_last_kernel_name -- static name of the kernel family the last
- * successful attn_fwd/attn_fwd_ex call on this host thread enqueued
- * ("prefill_tcgen05_d64_bf16", "decode_split_d64_bf16+decode_combine", ...
- * or "none" for an empty call), so a benchmark can record which kernel ran.
+ * successful attn_fwd/attn_fwd_ex/attn_fwd_gqa/attn_bwd call on this host
+ * thread enqueued ("prefill_tcgen05_d64_bf16",
+ * "decode_split_d64_bf16+decode_combine", ... or "none" for an empty call),
+ * so a benchmark can record which kernel ran.
  */
 const char* attn_last_kernel_name(void);
+
+/*
+ * attn_bwd -- gradients of attn_fwd: dq, dk, dv from q, k, v, the forward's
+ * o and lse, and dout = dL/dO.
+ *
+ * The backward pass recomputes the probabilities tile by tile from q, k and
+ * the saved lse instead of reading a stored probability matrix ("IO-Aware
+ * Attention: Tiling the Score Matrix Without Materializing It", section
+ * "What has to stay in fast memory": the saved state is O(n d) per head plus
+ * the O(n) row constants). The pages print no gradient formulas; these are
+ * the derivative of the forward definition above. With P_ij =
+ * exp(scale * q_i . k_j - lse_i) on visible pairs (0 elsewhere):
+ *     dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  D_i = dO_i . o_i,
+ *     dQ = scale * dS K,  dK = scale * dS^T Q.
+ *
+ * Arguments: q, o, dout: [B][h][T_q][d]; k, v: [B][h][T_kv][d]; lse: fp32
+ * [B][h][T_q] as written by attn_fwd for the same q, k, v, scale and causal
+ * flag; dq: [B][h][T_q][d], dk, dv: [B][h][T_kv][d], written (not
+ * accumulated into), in the 16-bit dtype, rounded once from fp32 sums.
+ * scale, causal, dtype and the supported set as for attn_fwd (T_q == 1 is
+ * allowed). Pointer rules as for attn_fwd; dq, dk, dv must not overlap each
+ * other or any input. workspace: device memory of at least
+ * attn_bwd_workspace_bytes(B, h, T_q, T_kv, d) bytes, 16-byte aligned, not
+ * overlapping any argument; pass NULL with workspace_bytes 0 to have the
+ * library take it stream-ordered (cudaMallocAsync/cudaFreeAsync on stream).
+ * Deterministic: no atomics, the same inputs give the same bits.
+ * Returns ATTN_ERR_WORKSPACE for a missing, short, misaligned or
+ * overlapping workspace; otherwise as attn_fwd.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int h, int T_q, int T_kv, int d, float scale, int causal, int dtype,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd_gqa -- attn_bwd for grouped-query attention (attn_fwd_gqa):
+ * q, o, dout, dq: [B][h_q][T_q][d]; k, v, dk, dv: [B][h_kv][T_kv][d]. The
+ * gradient of a key/value head is the sum over the h_q/h_kv query heads that
+ * read it, formed in one pass (no atomics). h_kv == h_q is attn_bwd.
+ */
+attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           int B, int h_q, int h_kv, int T_q, int T_kv, int d, float scale,
+                           int causal, int dtype, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * attn_bwd_workspace_bytes -- workspace attn_bwd / attn_bwd_gqa need: two
+ * fp32 row terms per query row, rows padded to 128 per head:
+ * 8 * B * h_q * roundup(T_q, 128) bytes (0 for invalid or empty sizes).
+ */
+size_t attn_bwd_workspace_bytes(int B, int h, int T_q, int T_kv, int d);
 
 /*
  * attn_fwd_decode_noalloc -- the decode path (T_q == 1) without any

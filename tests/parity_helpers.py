@@ -111,3 +111,107 @@ def sample_rows(T_q, n_random=12, seed=0):
     rows = [r for r in fixed if 0 <= r < T_q]
     rows += list(rng.integers(0, T_q, size=n_random))
     return np.unique(np.array(rows, dtype=np.int64))
+
+
+
+# ---------------------------------------------------------------------------
+# Backward pass
+# ---------------------------------------------------------------------------
+# Gate for the gradients, from the arithmetic of the kernels (all sums fp32):
+#   dV_j = sum_i P_ij dO_i:  P rounded once to 16 bits (u P_ij) and dV
+#        rounded once at the end (u |dV_j|);
+#   dK_j = scale sum_i dS_ij Q_i and dQ_i = scale sum_j dS_ij K_j: dS rounded
+#        once to 16 bits (u |dS_ij|); D_i = dO_i . o_i is formed from the
+#        16-bit forward output o (u sum_c |dO_ic o_ic|, entering dS_ij times
+#        P_ij); the result rounded once (u |X|).
+# The fp32 sums over up to a few thousand terms add well under u for bf16
+# and about u/2 for fp16, hence the factor 2. fp16 P and dS below the
+# smallest normal (6.1e-5) keep an absolute precision of 2^-25, added as a
+# term of its own.
+BWD_FACTOR = 2.0
+
+
+def gpu_bwd(q, k, v, do, causal, scale=None, workspace=None, o_lse=None):
+    """Forward (for o and lse, unless given) then backward on the GPU.
+    q, k, v, do: CPU 16-bit tensors. Returns float64 numpy (dq, dk, dv)."""
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    h_q, h_kv = q.shape[1], k.shape[1]
+    if o_lse is None:
+        if h_q == h_kv:
+            o, lse = _lib.attn_fwd(qd, kd, vd, scale=scale, causal=causal)
+        else:
+            o, lse = _lib.attn_fwd_gqa(qd, kd, vd, scale=scale, causal=causal)
+    else:
+        o, lse = (t.to(dev) for t in o_lse)
+    grads = [torch.full_like(t, float("nan")) for t in (qd, kd, vd)]   # unwritten shows up
+    _lib.attn_bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal, dq=grads[0], dk=grads[1],
+                  dv=grads[2], workspace=workspace)
+    torch.cuda.synchronize()
+    st, word = _lib.get_device_error()
+    assert st == _lib.ATTN_OK, f"device status {st} word {word:#x}"
+    return tuple(g.double().cpu().numpy() for g in grads)
+
+
+def oracle_bwd(q, k, v, do, causal, scale=None):
+    """(dq, dk, dv) from the oracle, the magnitude terms the gate scales by u
+    and the fp16 subnormal floor, all float64 numpy."""
+    d = q.shape[-1]
+    s = oracle_scale(d ** -0.5 if scale is None else scale)
+    qn, kn, vn, dn = (t.double().numpy() for t in (q, k, v, do))
+    B, h_q, T_q, _ = qn.shape
+    h_kv = kn.shape[1]
+    g = h_q // h_kv
+    if h_q == h_kv:
+        ref = oracle.attention_backward(qn, kn, vn, dn, scale=s, causal=causal)
+    else:
+        ref = oracle.gqa_attention_backward(qn, kn, vn, dn, scale=s, causal=causal)
+    a_dq = np.zeros_like(qn)
+    a_dk = np.zeros_like(kn)
+    a_dv = np.zeros_like(vn)
+    f_dq = np.zeros_like(qn)
+    f_dk = np.zeros_like(kn)
+    f_dv = np.zeros_like(vn)
+    o_ref, _ = oracle.standard_attention(qn, np.repeat(kn, g, axis=1), np.repeat(vn, g, axis=1),
+                                         scale=s, causal=causal)
+    T_kv = kn.shape[2]
+    vis = oracle.causal_visible(T_q, T_kv) if causal else np.ones((T_q, T_kv), dtype=bool)
+    # fp16 values below the smallest normal keep an absolute precision of 2^-25
+    sub = 2.0 ** -25 if q.dtype == torch.float16 else 0.0
+    for b in range(B):
+        for hq in range(h_q):
+            hk = hq // g
+            sc = s * (qn[b, hq] @ kn[b, hk].T)
+            sc = np.where(vis, sc, -np.inf)
+            e = np.exp(sc - sc.max(axis=1, keepdims=True))
+            p = e / e.sum(axis=1, keepdims=True)
+            dp = dn[b, hq] @ vn[b, hk].T
+            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+            r = (np.abs(dn[b, hq]) * np.abs(o_ref[b, hq])).sum(axis=1)   # sum_c |dO_ic o_ic|
+            aq, ak, ado = np.abs(qn[b, hq]), np.abs(kn[b, hk]), np.abs(dn[b, hq])
+            a_dv[b, hk] += p.T @ ado
+            a_dk[b, hk] += s * (np.abs(ds).T @ aq + (p * r[:, None]).T @ aq)
+            a_dq[b, hq] = s * (np.abs(ds) @ ak + r[:, None] * (p @ ak))
+            f_dv[b, hk] += sub * (vis.T.astype(np.float64) @ ado)
+            f_dk[b, hk] += s * sub * (vis.T.astype(np.float64) @ aq)
+            f_dq[b, hq] = s * sub * (vis.astype(np.float64) @ ak)
+    return ref, (a_dq, a_dk, a_dv), (f_dq, f_dk, f_dv)
+
+
+def compare_grads(got, reference, dtype, what=""):
+    """Element-wise gate on dq, dk, dv against oracle_bwd's output; returns
+    the worst error/bound ratio."""
+    ref, mag, floor = reference
+    u = UNIT_ROUNDOFF[dtype]
+    worst_ratio = 0.0
+    for name, x, r, a, f in zip(("dq", "dk", "dv"), got, ref, mag, floor):
+        assert np.isfinite(x).all(), f"{what}: {name} has non-finite (unwritten or NaN) elements"
+        err = np.abs(x - r)
+        bound = BWD_FACTOR * (u * (a + np.abs(r)) + f) + 1e-6
+        ratio = err / bound
+        i = int(np.argmax(ratio))
+        assert ratio.flat[i] <= 1.0, (
+            f"{what}: {name} element {np.unravel_index(i, x.shape)} = {x.flat[i]:.6g}, oracle "
+            f"{r.flat[i]:.6g}, off by {err.flat[i]:.3e} > bound {bound.flat[i]:.3e}")
+        worst_ratio = max(worst_ratio, float(ratio.flat[i]))
+    return worst_ratio

@@ -209,3 +209,64 @@ def test_gqa_workspace_bytes(L):
     assert _lib.gqa_workspace_bytes(2, 8, 2, 300, 300, 64, 16) == 0     # prefill
     assert _lib.gqa_workspace_bytes(2, 8, 3, 1, 300, 64, 16) == 0       # invalid grouping
     assert _lib.gqa_workspace_bytes(2, 8, 8, 1, 300, 64, 0) == _lib.workspace_bytes(2, 8, 1, 300, 64, 0)
+
+
+# backward: fake addresses for the extra tensors, spaced like the others
+DO, DQ, DK, DV = (0x100000 * i for i in range(7, 11))
+
+
+def _bwd(h_kv=None, **over):
+    a = dict(GOOD)
+    ptrs = dict(q=Q, k=K, v=V, o=O, do=DO, lse=LSE, dq=DQ, dk=DK, dv=DV)
+    for key in list(over):
+        if key in ptrs:
+            ptrs[key] = over.pop(key)
+    ws, nbytes = over.pop("ws", None), over.pop("nbytes", 0)
+    a.update(over)
+    return _lib.bwd_raw(ptrs["q"], ptrs["k"], ptrs["v"], ptrs["o"], ptrs["do"], ptrs["lse"],
+                        ptrs["dq"], ptrs["dk"], ptrs["dv"], a["B"], a["h"],
+                        a["h"] if h_kv is None else h_kv, a["T_q"], a["T_kv"], a["d"], a["scale"],
+                        a["causal"], a["dtype"], ws, nbytes, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(do=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dq=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dk=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dv=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(q=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dq=DQ + 8), _lib.ATTN_ERR_INVALID_ARG),              # misaligned
+    (dict(do=DO + 4), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dq=Q), _lib.ATTN_ERR_INVALID_ARG),                   # gradient aliases an input
+    (dict(dk=DO + 64), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dv=LSE), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dv=DK + 16), _lib.ATTN_ERR_INVALID_ARG),             # gradients overlap each other
+    (dict(d=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(T_q=300, T_kv=200), _lib.ATTN_ERR_INVALID_ARG),     # causal needs T_q <= T_kv
+    (dict(scale=0.0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=3), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(ws=WS, nbytes=16), _lib.ATTN_ERR_WORKSPACE),         # too small
+    (dict(ws=WS + 4, nbytes=1 << 20), _lib.ATTN_ERR_WORKSPACE),  # misaligned
+    (dict(ws=DQ, nbytes=1 << 20), _lib.ATTN_ERR_WORKSPACE),    # overlaps a gradient
+    (dict(ws=0, nbytes=1 << 20), _lib.ATTN_ERR_WORKSPACE),     # size without a buffer
+    (dict(B=0), _lib.ATTN_OK),                                 # empty
+    (dict(T_q=0), _lib.ATTN_OK),
+])
+def test_backward_arguments(L, over, status):
+    assert _bwd(**over) == status
+
+
+@pytest.mark.parametrize("h_kv,status", [(0, _lib.ATTN_ERR_INVALID_ARG),
+                                         (2, _lib.ATTN_ERR_INVALID_ARG),   # 3 heads, 2 kv heads
+                                         (6, _lib.ATTN_ERR_INVALID_ARG)])
+def test_backward_gqa_grouping(L, h_kv, status):
+    assert _bwd(h_kv=h_kv) == status
+
+
+def test_backward_workspace_bytes(L):
+    # two fp32 row terms per query row, rows padded to 128 per head
+    assert _lib.bwd_workspace_bytes(2, 3, 100, 200, 64) == 2 * 2 * 3 * 128 * 4
+    assert _lib.bwd_workspace_bytes(1, 1, 129, 129, 128) == 2 * 256 * 4
+    assert _lib.bwd_workspace_bytes(1, 1, 100, 100, 96) == 0
+    assert _lib.bwd_workspace_bytes(0, 1, 100, 100, 64) == 0
