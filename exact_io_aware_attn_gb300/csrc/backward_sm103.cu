@@ -22,14 +22,17 @@
 //                CTA streams 64-key tiles of K and V (causal: up to the
 //                diagonal) and accumulates dQ in tensor memory
 //
-// Both modes are one kernel template. Roles (192 threads): warps 0-3 own
-// TMEM lanes 0-127 (one resident row each) and turn scores into P and dS;
-// warp 4 is the TMA producer; warp 5 owns TMEM and issues the MMAs. Per
-// streamed tile t the tensor core computes
+// Both modes are one kernel template. Roles (320 threads): warps 0-7 turn
+// scores into P and dS -- warp w owns TMEM lanes 32*(w%4).. (one resident row
+// per thread) and columns 32*(w/4).. of each 64-column score tile, so every
+// sub-partition runs two of them; warp 8 is the TMA producer; warp 9 owns TMEM
+// and issues the MMAs. Per streamed tile t the tensor core computes
 //   S_t  = X U_t^T and dP_t = Y W_t^T      (M=128 resident rows, N=64, K=d)
-// into one of two TMEM buffers, the elementwise warps store P_t and dS_t as
-// 16-bit over the first 32 columns of S_t and dP_t, and the tensor core then
-// accumulates (A read from TMEM, B the streamed tile read MN-major)
+// into one of two TMEM buffers; each elementwise warp stores its 32 columns
+// of P_t and dS_t as 16-bit pairs over the first 16 columns of its own half
+// of S_t and dP_t (so no warp overwrites columns another warp still reads),
+// and the tensor core then accumulates (A read from TMEM, B the streamed
+// tile read MN-major)
 //   KV mode (X=K, Y=V, U=Q, W=dO):  dV += P_t^T dO_t,  dK += dS_t^T Q_t
 //   Q mode  (X=Q, Y=dO, U=K, W=V):  dQ += dS_t K_t
 // The scores of tile t+1 go into the other buffer while the elementwise warps
@@ -58,9 +61,10 @@ constexpr int kRes = 128;              // resident rows per CTA (TMEM lanes, M o
 constexpr int kStr = 64;               // rows of one streamed tile
 constexpr int kSubRes = kRes * 128;    // one [128 rows][64 x 16-bit] swizzled sub-tile
 constexpr int kSubStr = kStr * 128;    // one [64 rows][64 x 16-bit] swizzled sub-tile
-constexpr int kBwdThreads = 192;
-constexpr int kWarpProd = 4;
-constexpr int kWarpMma = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kWarpProd = 8;
+constexpr int kWarpMma = 9;
+constexpr int kEltThreads = 256;       // warps 0-7
 constexpr uint32_t kColAcc1 = 256;     // dV (KV mode)
 
 template <int D, bool KV>
@@ -74,13 +78,23 @@ struct BwdCfg {
   static constexpr int OFF_Y = RES_BYTES;
   static constexpr int OFF_RING = 2 * RES_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * STAGE_BYTES;
-  // res_full, stage_full[ST], stage_empty[ST], sp_full[2], p_full[2], acc_full, mma_done
-  static constexpr int N_BARS = 1 + 2 * STAGES + 6;
+  // res_full, stage_full[ST], stage_empty[ST], sp_full[2], p_full[2], acc_full, mma_done,
+  // res_tmem
+  static constexpr int N_BARS = 1 + 2 * STAGES + 7;
   static constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_ACC2 = 256u + D;             // dK (KV mode) or dQ (Q mode)
+  // The resident tiles X and Y also go to TMEM (D/2 columns each), so the
+  // score products read A from TMEM and only B from shared memory -- except
+  // dK/dV at d = 128, where TMEM is full (buffers 256 + dV 128 + dK 128).
+  static constexpr bool XY_TMEM = !(KV && D == 128);
+  static constexpr uint32_t COL_X = KV ? 256u + 2u * D : 256u;  // Q mode: the unused dV columns
+  static constexpr uint32_t COL_Y = COL_X + D / 2;
 };
+static_assert(BwdCfg<64, true>::COL_Y + 32 <= 512, "tensor memory");
+static_assert(BwdCfg<128, false>::COL_Y + 64 <= BwdCfg<128, false>::COL_ACC2, "tensor memory");
+static_assert(BwdCfg<64, false>::COL_Y + 32 <= BwdCfg<64, false>::COL_ACC2, "tensor memory");
 static_assert(BwdCfg<128, true>::SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(BwdCfg<128, false>::SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(BwdCfg<128, true>::COL_ACC2 + 128 <= 512, "tensor memory");
@@ -88,7 +102,8 @@ static_assert(BwdCfg<128, true>::COL_ACC2 + 128 <= 512, "tensor memory");
 __host__ __device__ constexpr uint32_t col_buf(int b) { return static_cast<uint32_t>(b) * 128u; }
 
 enum : uint32_t {
-  kSiteProdStage = 1, kSiteMmaRes, kSiteMmaStage, kSiteMmaP, kSiteEltS, kSiteEltStage, kSiteEltAcc
+  kSiteProdStage = 1, kSiteMmaRes, kSiteMmaStage, kSiteMmaP, kSiteEltS, kSiteEltStage, kSiteEltAcc,
+  kSiteEltRes
 };
 
 template <bool BF16>
@@ -246,6 +261,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* p_full = sp_full + 2;
   uint64_t* acc_full = p_full + 2;
   uint64_t* mma_done = acc_full + 1;
+  uint64_t* res_tmem = mma_done + 1;   // X and Y copied into TMEM (XY_TMEM)
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMPTR);
 
   const int warp = threadIdx.x >> 5;
@@ -263,10 +279,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&sp_full[b], 1);
-      ptx::mbar_init(&p_full[b], 128);
+      ptx::mbar_init(&p_full[b], kEltThreads);
     }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(res_tmem, kEltThreads);
     ptx::fence_mbarrier_init();
   }
   if (warp == kWarpMma) {
@@ -329,85 +346,112 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kRes, kStr, false, false);
-      constexpr uint32_t idG = ptx::make_idesc_f16(BF16, kRes, D, false, true);
-      const uint32_t sX = ptx::smem_u32(smem + C::OFF_X);
-      const uint32_t sY = ptx::smem_u32(smem + C::OFF_Y);
-      const uint32_t sR = ptx::smem_u32(smem + C::OFF_RING);
-      // K-major views (score products) and MN-major views (gradient products)
-      const uint64_t dX = ptx::make_sdesc_sw128(sX, 16, 1024);
-      const uint64_t dY = ptx::make_sdesc_sw128(sY, 16, 1024);
-      const uint64_t dUk = ptx::make_sdesc_sw128(sR, 16, 1024);
-      const uint64_t dWk = ptx::make_sdesc_sw128(sR + C::STR_BYTES, 16, 1024);
-      const uint64_t dUm = ptx::make_sdesc_sw128(sR, kSubStr, 1024);
-      const uint64_t dWm = ptx::make_sdesc_sw128(sR + C::STR_BYTES, kSubStr, 1024);
+    // The whole warp runs this loop in uniform control flow (so descriptor
+    // arithmetic stays warp-uniform); one elected lane issues each batch of
+    // MMAs and its commit. elect.sync picks the lowest active lane, the same
+    // lane every time, so every commit covers that lane's earlier MMAs.
+    constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kRes, kStr, false, false);
+    constexpr uint32_t idG = ptx::make_idesc_f16(BF16, kRes, D, false, true);
+    const uint32_t sX = ptx::smem_u32(smem + C::OFF_X);
+    const uint32_t sY = ptx::smem_u32(smem + C::OFF_Y);
+    const uint32_t sR = ptx::smem_u32(smem + C::OFF_RING);
+    // K-major views (score products) and MN-major views (gradient products)
+    const uint64_t dX = ptx::make_sdesc_sw128(sX, 16, 1024);
+    const uint64_t dY = ptx::make_sdesc_sw128(sY, 16, 1024);
+    const uint64_t dUk = ptx::make_sdesc_sw128(sR, 16, 1024);
+    const uint64_t dWk = ptx::make_sdesc_sw128(sR + C::STR_BYTES, 16, 1024);
+    const uint64_t dUm = ptx::make_sdesc_sw128(sR, kSubStr, 1024);
+    const uint64_t dWm = ptx::make_sdesc_sw128(sR + C::STR_BYTES, kSubStr, 1024);
 
-      auto issue_scores = [&](int b, int slot) {
-        const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
-        const uint32_t d_s = tmem + col_buf(b);
+    auto issue_scores = [&](int b, int slot) {
+      const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
+      const uint64_t u0 = dUk + so, w0 = dWk + so;
+      const uint32_t d_s = tmem + col_buf(b);
+      if (ptx::elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ro = (kk >> 2) * kSubRes + (kk & 3) * 32;
           const uint32_t to = (kk >> 2) * kSubStr + (kk & 3) * 32;
-          ptx::mma_f16_ss(d_s, dX + (ro >> 4), dUk + so + (to >> 4), idS, kk > 0 ? 1u : 0u);
+          if constexpr (C::XY_TMEM)
+            ptx::mma_f16_ts(d_s, tmem + C::COL_X + kk * 8, u0 + (to >> 4), idS, kk > 0 ? 1u : 0u);
+          else
+            ptx::mma_f16_ss(d_s, dX + (ro >> 4), u0 + (to >> 4), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ro = (kk >> 2) * kSubRes + (kk & 3) * 32;
           const uint32_t to = (kk >> 2) * kSubStr + (kk & 3) * 32;
-          ptx::mma_f16_ss(d_s + 64, dY + (ro >> 4), dWk + so + (to >> 4), idS, kk > 0 ? 1u : 0u);
+          if constexpr (C::XY_TMEM)
+            ptx::mma_f16_ts(d_s + 64, tmem + C::COL_Y + kk * 8, w0 + (to >> 4), idS,
+                            kk > 0 ? 1u : 0u);
+          else
+            ptx::mma_f16_ss(d_s + 64, dY + (ro >> 4), w0 + (to >> 4), idS, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&sp_full[b]);
-      };
-      auto issue_grads = [&](int b, int slot, bool first) {
-        const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
+      }
+      __syncwarp();
+    };
+    auto issue_grads = [&](int b, int slot, bool first) {
+      const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
+      const uint64_t u0 = dUm + so, w0 = dWm + so;
+      const uint32_t a0 = tmem + col_buf(b);
+      if (ptx::elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < kStr / 16; ++kk) {
           const uint64_t bo = static_cast<uint64_t>(kk * 16 * 128) >> 4;  // 16 streamed rows
           const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
-          if constexpr (KV)
-            ptx::mma_f16_ts(tmem + kColAcc1, tmem + col_buf(b) + kk * 8, dWm + so + bo, idG, acc);
-          ptx::mma_f16_ts(tmem + C::COL_ACC2, tmem + col_buf(b) + 64 + kk * 8, dUm + so + bo, idG,
-                          acc);
+          // streamed rows 16kk..16kk+15: half kk/2, 16-bit pairs from column 8*(kk%2)
+          const uint32_t a_col = a0 + (kk >> 1) * 32 + (kk & 1) * 8;
+          if constexpr (KV) ptx::mma_f16_ts(tmem + kColAcc1, a_col, w0 + bo, idG, acc);
+          ptx::mma_f16_ts(tmem + C::COL_ACC2, a_col + 64, u0 + bo, idG, acc);
         }
         ptx::mma_commit(&stage_empty[slot]);
-      };
-
-      bool ok = ptx::mbar_wait(res_full, 0, status, status_word(kKern, kSiteMmaRes));
-      if (ok)
-        ok = ptx::mbar_wait(&stage_full[0], 0, status, status_word(kKern, kSiteMmaStage));
-      if (ok) {
-        ptx::tc_fence_after();
-        issue_scores(0, 0);
       }
-      for (int it = 0; ok && it < n; ++it) {
-        const int b = it & 1;
-        if (it + 1 < n) {
-          // scores of the next tile into the other buffer: its previous
-          // contents (tile it-1) were read by tile it-1's gradient products,
-          // issued earlier by this thread and so executed earlier
-          const int s1 = (it + 1) % ST;
-          ok = ptx::mbar_wait(&stage_full[s1], ((it + 1) / ST) & 1, status,
-                              status_word(kKern, kSiteMmaStage));
-          if (!ok) break;
-          ptx::tc_fence_after();
-          issue_scores(b ^ 1, s1);
-        }
-        ok = ptx::mbar_wait(&p_full[b], (it >> 1) & 1, status, status_word(kKern, kSiteMmaP));
+      __syncwarp();
+    };
+    // every lane waits; the result is made warp-uniform
+    auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      const bool good = ptx::mbar_wait(bar, parity, status, status_word(kKern, site));
+      return __all_sync(0xffffffffu, good);
+    };
+
+    bool ok = C::XY_TMEM ? wait(res_tmem, 0, kSiteMmaRes) : wait(res_full, 0, kSiteMmaRes);
+    if (ok) ok = wait(&stage_full[0], 0, kSiteMmaStage);
+    if (ok) {
+      ptx::tc_fence_after();
+      issue_scores(0, 0);
+    }
+    for (int it = 0; ok && it < n; ++it) {
+      const int b = it & 1;
+      if (it + 1 < n) {
+        // scores of the next tile into the other buffer: its previous
+        // contents (tile it-1) were read by tile it-1's gradient products,
+        // issued earlier by the same lane and so executed earlier
+        const int s1 = (it + 1) % ST;
+        ok = wait(&stage_full[s1], ((it + 1) / ST) & 1, kSiteMmaStage);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_grads(b, it % ST, it == 0);
+        issue_scores(b ^ 1, s1);
       }
-      if (ok) ptx::mma_commit(acc_full);
-      // every MMA this thread issued must be complete before TMEM is freed
-      ptx::mma_commit(mma_done);
-      mbar_drain(mma_done, 0);
+      ok = wait(&p_full[b], (it >> 1) & 1, kSiteMmaP);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_grads(b, it % ST, it == 0);
     }
+    // every MMA issued must be complete before TMEM is freed
+    if (ptx::elect_one_sync()) {
+      if (ok) ptx::mma_commit(acc_full);
+      ptx::mma_commit(mma_done);
+    }
+    __syncwarp();
+    mbar_drain(mma_done, 0);
   } else {
     // ---------------------------------------------------------------- elementwise
-    const int row = warp * 32 + lane;                  // TMEM lane = resident row
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int quarter = warp & 3;                      // TMEM lanes 32*quarter..
+    const int half = warp >> 2;                        // columns 32*half.. of each tile
+    const int row = quarter * 32 + lane;               // TMEM lane = resident row
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t t_half = t_lane + static_cast<uint32_t>(half * 32);
     const int rrow = w.r0 + row;                       // KV: key index; Q: query row
     float l2_row = 0.f, dd_row = 0.f;
     if constexpr (!KV) {
@@ -415,7 +459,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       l2_row = ws_l2[ro];
       dd_row = ws_dd[ro];
     }
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
     bool ok = true;
+    if constexpr (C::XY_TMEM) {
+      // row `row` of X (warps 0-3) or Y (warps 4-7), from the 128-byte
+      // swizzled tile (16-byte chunk c of a row r sits at chunk c ^ (r % 8)),
+      // into D/2 columns of TMEM as 16-bit pairs in K order: the A-operand
+      // layout of the score products
+      ok = ptx::mbar_wait(res_full, 0, status, status_word(kKern, kSiteEltRes));
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        const uint8_t* tile = smem + (half ? C::OFF_Y : C::OFF_X);
+#pragma unroll
+        for (int c32 = 0; c32 < D / 64; ++c32) {   // 32 columns = one 64-element sub-tile
+          uint32_t words[32];
+          const uint8_t* sub = tile + c32 * kSubRes + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sub + ((c ^ (row & 7)) << 4));
+            words[4 * c] = v.x;
+            words[4 * c + 1] = v.y;
+            words[4 * c + 2] = v.z;
+            words[4 * c + 3] = v.w;
+          }
+          ptx::tmem_st_32x32b_x32(t_lane + (half ? C::COL_Y : C::COL_X) + c32 * 32, words);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(res_tmem);
+      }
+    }
     for (int it = 0; ok && it < n; ++it) {
       const int b = it & 1;
       const int slot = it % ST;
@@ -432,63 +505,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      uint32_t sr[64], pr[64];
-      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b) + 64, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
-      ptx::tmem_ld_32x32b_x32(t_lane + col_buf(b) + 96, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+      uint32_t sr[64];
+      ptx::tmem_ld_32x32b_x32(t_half + col_buf(b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      ptx::tmem_ld_32x32b_x32(t_half + col_buf(b) + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld_64(sr);
-      tmem_wait_ld_64(pr);
-      const float* s = reinterpret_cast<const float*>(sr);
-      const float* dp = reinterpret_cast<const float*>(pr);
+      const float* s = reinterpret_cast<const float*>(sr);        // scores, 32 columns
+      const float* dp = reinterpret_cast<const float*>(sr + 32);  // dP, same columns
 
       int sbh, s0;
       bwd_item(w, it, &sbh, &s0);
+      s0 += half * 32;  // streamed row of this warp's column 0
       // columns [cmin, cmax] of this row are visible
       int cmin, cmax;
       if constexpr (KV) {
         cmin = causal ? rrow - off - s0 : INT_MIN / 2;   // query s0+c sees key rrow iff c >= cmin
-        cmax = kStr - 1;
-        if (rrow >= T_kv) cmin = kStr;                   // key past the end: nothing visible
+        cmax = 31;
+        if (rrow >= T_kv) cmin = 32;                     // key past the end: nothing visible
       } else {
         cmin = 0;
         cmax = (causal ? min(rrow + off, T_kv - 1) : T_kv - 1) - s0;
       }
-      const bool all_visible = __all_sync(0xffffffffu, cmin <= 0 && cmax >= kStr - 1);
-      const float* vl2 = nullptr;
-      const float* vdd = nullptr;
+      const bool all_visible = __all_sync(0xffffffffu, cmin <= 0 && cmax >= 31);
+      const float4* vl2 = nullptr;
+      const float4* vdd = nullptr;
       if constexpr (KV) {
-        vl2 = reinterpret_cast<const float*>(smem + C::OFF_RING + slot * C::STAGE_BYTES +
-                                             2 * C::STR_BYTES);
-        vdd = vl2 + kStr;
+        const float* v0 = reinterpret_cast<const float*>(smem + C::OFF_RING +
+                                                         slot * C::STAGE_BYTES + 2 * C::STR_BYTES);
+        vl2 = reinterpret_cast<const float4*>(v0 + half * 32);
+        vdd = reinterpret_cast<const float4*>(v0 + kStr + half * 32);
       }
-      uint32_t pk[32], gk[32];
+      // three passes without branches inside, so the 32 columns' chains
+      // interleave: exponentials, then (diagonal tiles only) the mask, then
+      // dS and the 16-bit pairs
+      float2 pp[16];
 #pragma unroll
-      for (int c = 0; c < kStr; c += 2) {
-        float la, lb, da, db;
+      for (int c4 = 0; c4 < 8; ++c4) {
+        float4 l;
         if constexpr (KV) {
-          const float2 l = *reinterpret_cast<const float2*>(vl2 + c);
-          const float2 dv = *reinterpret_cast<const float2*>(vdd + c);
-          la = l.x;
-          lb = l.y;
-          da = dv.x;
-          db = dv.y;
+          l = vl2[c4];
         } else {
-          la = lb = l2_row;
-          da = db = dd_row;
+          l = make_float4(l2_row, l2_row, l2_row, l2_row);
         }
-        float pa = ptx::ex2_approx(fmaf(s[c], scale_log2, -la));
-        float pb = ptx::ex2_approx(fmaf(s[c + 1], scale_log2, -lb));
-        if (!all_visible) {
-          pa = (c >= cmin && c <= cmax) ? pa : 0.f;
-          pb = (c + 1 >= cmin && c + 1 <= cmax) ? pb : 0.f;
-        }
-        pk[c >> 1] = pack2<BF16>(pa, pb);
-        gk[c >> 1] = pack2<BF16>(pa * (dp[c] - da), pb * (dp[c + 1] - db));
+        const float2 x0 = __ffma2_rn(make_float2(s[4 * c4], s[4 * c4 + 1]), sl2, make_float2(-l.x, -l.y));
+        const float2 x1 =
+            __ffma2_rn(make_float2(s[4 * c4 + 2], s[4 * c4 + 3]), sl2, make_float2(-l.z, -l.w));
+        pp[2 * c4] = make_float2(ptx::ex2_approx(x0.x), ptx::ex2_approx(x0.y));
+        pp[2 * c4 + 1] = make_float2(ptx::ex2_approx(x1.x), ptx::ex2_approx(x1.y));
       }
-      // P over the first 32 columns of S, dS over the first 32 of dP
-      ptx::tmem_st_32x32b_x32(t_lane + col_buf(b), pk);
-      ptx::tmem_st_32x32b_x32(t_lane + col_buf(b) + 64, gk);
+      if (!all_visible) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          pp[c >> 1].x = (c >= cmin && c <= cmax) ? pp[c >> 1].x : 0.f;
+          pp[c >> 1].y = (c + 1 >= cmin && c + 1 <= cmax) ? pp[c >> 1].y : 0.f;
+        }
+      }
+      uint32_t pk[16], gk[16];
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        float4 dd;
+        if constexpr (KV) {
+          dd = vdd[c4];
+        } else {
+          dd = make_float4(dd_row, dd_row, dd_row, dd_row);
+        }
+        const float2 g0 = __fmul2_rn(pp[2 * c4], __fadd2_rn(make_float2(dp[4 * c4], dp[4 * c4 + 1]),
+                                                             make_float2(-dd.x, -dd.y)));
+        const float2 g1 = __fmul2_rn(pp[2 * c4 + 1], __fadd2_rn(make_float2(dp[4 * c4 + 2], dp[4 * c4 + 3]),
+                                                                 make_float2(-dd.z, -dd.w)));
+        pk[2 * c4] = pack2<BF16>(pp[2 * c4].x, pp[2 * c4].y);
+        pk[2 * c4 + 1] = pack2<BF16>(pp[2 * c4 + 1].x, pp[2 * c4 + 1].y);
+        gk[2 * c4] = pack2<BF16>(g0.x, g0.y);
+        gk[2 * c4 + 1] = pack2<BF16>(g1.x, g1.y);
+      }
+      // P over the first 16 columns of this warp's half of S, dS likewise in dP
+      ptx::tmem_st_32x32b_x16(t_half + col_buf(b), pk);
+      ptx::tmem_st_32x32b_x16(t_half + col_buf(b) + 64, gk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&p_full[b]);
@@ -501,14 +592,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tc_fence_after();
         const int T_out = KV ? T_kv : T_q;
         const bool write = rrow < T_out;
+        constexpr int HALF_D = D / 2;  // output columns of this warp
 #pragma unroll
         for (int a = KV ? 0 : 1; a < 2; ++a) {
           uint8_t* dst = reinterpret_cast<uint8_t*>(a == 0 ? out1 : out2) +
-                         (static_cast<size_t>(w.res_bh) * T_out + (write ? rrow : 0)) * D * 2;
+                         (static_cast<size_t>(w.res_bh) * T_out + (write ? rrow : 0)) * D * 2 +
+                         half * HALF_D * 2;
           const float mul = a == 0 ? 1.f : scale;
-          const uint32_t col = a == 0 ? kColAcc1 : C::COL_ACC2;
+          const uint32_t col = (a == 0 ? kColAcc1 : C::COL_ACC2) + half * HALF_D;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < HALF_D / 32; ++c) {
             uint32_t raw[32];
             ptx::tmem_ld_32x32b_x32(t_lane + col + c * 32, raw);
             tmem_wait_ld_32(raw);
