@@ -333,108 +333,122 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == kWarpMma) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kBM, kBN, false, false);
-        constexpr uint32_t idO = ptx::make_idesc_f16(BF16, kBM, D, false, true);
-        const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
-        const uint32_t sRing = ptx::smem_u32(smem + C::OFF_RING);
-        uint32_t g = 0, nq = 0;
-        uint32_t np[2] = {0, 0}, noe[2] = {0, 0};
-        bool ok = true;
+      // The whole warp runs this loop in uniform control flow, so descriptor
+      // arithmetic stays warp-uniform; one elected lane (the lowest active
+      // one, the same every time) issues each batch of MMAs and every commit,
+      // so each commit covers that lane's earlier MMAs.
+      constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kBM, kBN, false, false);
+      constexpr uint32_t idO = ptx::make_idesc_f16(BF16, kBM, D, false, true);
+      const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
+      const uint32_t sRing = ptx::smem_u32(smem + C::OFF_RING);
+      uint32_t g = 0, nq = 0;
+      uint32_t np[2] = {0, 0}, noe[2] = {0, 0};
+      bool ok = true;
 
-        auto wait_slot = [&](uint32_t idx) {
-          return ptx::mbar_wait(&slot_full[idx % SL], (idx / SL) & 1, status,
-                                status_word(kKernPrefill, kSiteMmaSlot));
-        };
-        const uint64_t desc_q0 = ptx::make_sdesc_sw128(sQ, 16, 1024);
-        const uint64_t desc_k0 = ptx::make_sdesc_sw128(sRing, 16, 1024);
-        const uint64_t desc_v0 = ptx::make_sdesc_sw128(sRing, kSub, 1024);
-        auto issue_s = [&](int x, uint32_t kslot) {
-          const uint64_t qd = desc_q0 + ((x * C::TILE_BYTES) >> 4);
-          const uint64_t kd = desc_k0 + ((kslot * C::TILE_BYTES) >> 4);
-          const uint32_t d_s = tmem + col_s(x);
+      auto wait_bar = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+        const bool good = ptx::mbar_wait(bar, parity, status, status_word(kKernPrefill, site));
+        return __all_sync(0xffffffffu, good);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (ptx::elect_one_sync()) ptx::mma_commit(bar);
+        __syncwarp();
+      };
+      auto wait_slot = [&](uint32_t idx) {
+        return wait_bar(&slot_full[idx % SL], (idx / SL) & 1, kSiteMmaSlot);
+      };
+      const uint64_t desc_q0 = ptx::make_sdesc_sw128(sQ, 16, 1024);
+      const uint64_t desc_k0 = ptx::make_sdesc_sw128(sRing, 16, 1024);
+      const uint64_t desc_v0 = ptx::make_sdesc_sw128(sRing, kSub, 1024);
+      auto issue_s = [&](int x, uint32_t kslot) {
+        const uint64_t qd = desc_q0 + ((x * C::TILE_BYTES) >> 4);
+        const uint64_t kd = desc_k0 + ((kslot * C::TILE_BYTES) >> 4);
+        const uint32_t d_s = tmem + col_s(x);
+        if (ptx::elect_one_sync()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * kSub + (kk & 3) * 32;
             ptx::mma_f16_ss(d_s, qd + (koff >> 4), kd + (koff >> 4), idS, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&s_full[x]);
-        };
-        auto issue_pv = [&](int x, uint32_t vslot, bool first) {
-          const uint64_t vd = desc_v0 + ((vslot * C::TILE_BYTES) >> 4);
-          const uint32_t d_o = tmem + col_o<D>(x);
-          const uint32_t a_p = tmem + col_s(x);
-          const uint32_t acc0 = first ? 0u : 1u;
+        }
+        __syncwarp();
+      };
+      auto issue_pv = [&](int x, uint32_t vslot, bool first) {
+        const uint64_t vd = desc_v0 + ((vslot * C::TILE_BYTES) >> 4);
+        const uint32_t d_o = tmem + col_o<D>(x);
+        const uint32_t a_p = tmem + col_s(x);
+        const uint32_t acc0 = first ? 0u : 1u;
+        if (ptx::elect_one_sync()) {
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            ptx::mma_f16_ts(d_o, a_p + kk * 8, vd + ((kk * 16 * 128) >> 4), idO, kk > 0 ? 1u : acc0);
-        };
-        auto wait_p = [&](int x, bool first) {
-          bool good = ptx::mbar_wait(&p_full[x], np[x] & 1, status,
-                                     status_word(kKernPrefill, kSiteMmaP));
-          ++np[x];
-          if (good && first) {
-            // O_X is overwritten by this unit's first product: the previous
-            // unit's epilogue must have read it.
-            good = ptx::mbar_wait(&o_empty[x], (noe[x] & 1) ^ 1, status,
-                                  status_word(kKernPrefill, kSiteMmaOEmpty));
-            ++noe[x];
-          }
-          ptx::tc_fence_after();
-          return good;
-        };
-
-        for (int r = 0; ok && r * G < U; ++r) {
-          const int u = unit_of_round(r, bid, G);
-          if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
-          ok = ptx::mbar_wait(q_full, nq & 1, status, status_word(kKernPrefill, kSiteMmaQ));
-          ++nq;
-          if (!ok) break;
-          // prologue: both score tiles of key tile 0
-          ok = wait_slot(g);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          issue_s(0, g % SL);
-          if (w.n_b > 0) issue_s(1, g % SL);
-          ptx::mma_commit(&slot_empty[g % SL]);
-          if (w.n_all == 1) ptx::mma_commit(q_empty);
-          for (int j = 0; j < w.n_all; ++j) {
-            const uint32_t vi = g + 2 * j + 1;  // V_j
-            const uint32_t ki = vi + 1;         // K_{j+1}
-            ok = wait_slot(vi);
-            if (!ok) break;
-            if (j < w.n_a) {
-              ok = wait_p(0, j == 0);
-              if (!ok) break;
-              issue_pv(0, vi % SL, j == 0);
-              if (j == w.n_a - 1) ptx::mma_commit(&o_full[0]);
-            }
-            if (j + 1 < w.n_all) {
-              ok = wait_slot(ki);
-              if (!ok) break;
-              ptx::tc_fence_after();
-              if (j + 1 < w.n_a) issue_s(0, ki % SL);
-            }
-            if (j < w.n_b) {
-              ok = wait_p(1, j == 0);
-              if (!ok) break;
-              issue_pv(1, vi % SL, j == 0);
-              if (j == w.n_b - 1) ptx::mma_commit(&o_full[1]);
-            }
-            ptx::mma_commit(&slot_empty[vi % SL]);
-            if (j + 1 < w.n_all) {
-              if (j + 1 < w.n_b) issue_s(1, ki % SL);
-              ptx::mma_commit(&slot_empty[ki % SL]);
-              if (j + 2 == w.n_all) ptx::mma_commit(q_empty);
-            }
-          }
-          g += 2 * w.n_all;
+            ptx::mma_f16_ts(d_o, a_p + kk * 8, vd + ((kk * 16 * 128) >> 4), idO,
+                            kk > 0 ? 1u : acc0);
         }
-        // All MMAs this thread issued must be complete before TMEM is freed.
-        ptx::mma_commit(mma_done);
-        mbar_drain(mma_done, 0);
+        __syncwarp();
+      };
+      auto wait_p = [&](int x, bool first) {
+        bool good = wait_bar(&p_full[x], np[x] & 1, kSiteMmaP);
+        ++np[x];
+        if (good && first) {
+          // O_X is overwritten by this unit's first product: the previous
+          // unit's epilogue must have read it.
+          good = wait_bar(&o_empty[x], (noe[x] & 1) ^ 1, kSiteMmaOEmpty);
+          ++noe[x];
+        }
+        ptx::tc_fence_after();
+        return good;
+      };
+
+      for (int r = 0; ok && r * G < U; ++r) {
+        const int u = unit_of_round(r, bid, G);
+        if (u >= U) continue;
+        const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
+        ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
+        ++nq;
+        if (!ok) break;
+        // prologue: both score tiles of key tile 0
+        ok = wait_slot(g);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_s(0, g % SL);
+        if (w.n_b > 0) issue_s(1, g % SL);
+        commit(&slot_empty[g % SL]);
+        if (w.n_all == 1) commit(q_empty);
+        for (int j = 0; j < w.n_all; ++j) {
+          const uint32_t vi = g + 2 * j + 1;  // V_j
+          const uint32_t ki = vi + 1;         // K_{j+1}
+          ok = wait_slot(vi);
+          if (!ok) break;
+          if (j < w.n_a) {
+            ok = wait_p(0, j == 0);
+            if (!ok) break;
+            issue_pv(0, vi % SL, j == 0);
+            if (j == w.n_a - 1) commit(&o_full[0]);
+          }
+          if (j + 1 < w.n_all) {
+            ok = wait_slot(ki);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            if (j + 1 < w.n_a) issue_s(0, ki % SL);
+          }
+          if (j < w.n_b) {
+            ok = wait_p(1, j == 0);
+            if (!ok) break;
+            issue_pv(1, vi % SL, j == 0);
+            if (j == w.n_b - 1) commit(&o_full[1]);
+          }
+          commit(&slot_empty[vi % SL]);
+          if (j + 1 < w.n_all) {
+            if (j + 1 < w.n_b) issue_s(1, ki % SL);
+            commit(&slot_empty[ki % SL]);
+            if (j + 2 == w.n_all) commit(q_empty);
+          }
+        }
+        g += 2 * w.n_all;
       }
+      // All MMAs this warp issued must be complete before TMEM is freed.
+      commit(mma_done);
+      mbar_drain(mma_done, 0);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
