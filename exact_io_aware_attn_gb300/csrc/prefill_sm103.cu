@@ -79,8 +79,8 @@ struct Cfg {
   static constexpr int OFF_RING = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_RING + SLOTS * TILE_BYTES;
   // q_full, q_empty, slot_full[S], slot_empty[S], s_full[2], p_full[2],
-  // o_full[2], o_empty[2], mma_done
-  static constexpr int N_BARS = 2 + 2 * SLOTS + 8 + 1;
+  // o_full[2], o_empty[2], mma_done, s_free[2], pv_done[2]
+  static constexpr int N_BARS = 2 + 2 * SLOTS + 8 + 1 + 4;
   static constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -88,6 +88,12 @@ struct Cfg {
   // use the special-function unit). Measured on GB300: the special-function
   // unit keeps up at both widths, so every pair uses it.
   static constexpr int POLY_PAIRS_OF_8 = 0;
+  // d = 64 leaves TMEM room (S 2x128 + O 2x64 = 384 columns) for P in
+  // columns of its own (2x64): S_X(j+1) can then be computed as soon as the
+  // softmax has read S_X(j), while P_X(j) and PV_X(j) are still in flight,
+  // which takes the MMA issue of PV_X(j) and S_X(j+1) off the softmax's
+  // critical path. d = 128 fills TMEM with S and O, and P overwrites S.
+  static constexpr bool SEP_P = (D == 64);
 };
 
 __host__ __device__ constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
@@ -95,11 +101,13 @@ template <int D>
 __host__ __device__ constexpr uint32_t col_o(int x) {
   return 256u + static_cast<uint32_t>(x) * static_cast<uint32_t>(D);
 }
+// P_X when it has columns of its own (SEP_P): after O_A and O_B
+__host__ __device__ constexpr uint32_t col_p(int x) { return 384u + static_cast<uint32_t>(x) * 64u; }
 
 // Wait sites recorded in the status word on a timeout.
 enum : uint32_t {
   kSiteProdQ = 1, kSiteProdSlot, kSiteMmaQ, kSiteMmaSlot, kSiteMmaP, kSiteMmaOEmpty,
-  kSiteSoftS, kSiteSoftO
+  kSiteSoftS, kSiteSoftO, kSiteMmaSFree, kSiteSoftPv
 };
 
 template <bool BF16>
@@ -240,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_full = p_full + 2;
   uint64_t* o_empty = o_full + 2;
   uint64_t* mma_done = o_empty + 2;
+  uint64_t* s_free = mma_done + 1;   // SEP_P: softmax X has read S_X (128 arrivals)
+  uint64_t* pv_done = s_free + 2;    // SEP_P: PV_X complete (P_X and O_X free)
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMPTR);
 
   const int warp = threadIdx.x >> 5;
@@ -263,6 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&o_empty[x], 128);
     }
     ptx::mbar_init(mma_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(&s_free[x], 128);
+      ptx::mbar_init(&pv_done[x], 1);
+    }
     ptx::fence_mbarrier_init();
   }
   if (warp == kWarpMma) {
@@ -399,52 +413,127 @@ __global__ void __launch_bounds__(kThreads, 1)
         return good;
       };
 
-      for (int r = 0; ok && r * G < U; ++r) {
-        const int u = unit_of_round(r, bid, G);
-        if (u >= U) continue;
-        const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
-        ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
-        ++nq;
-        if (!ok) break;
-        // prologue: both score tiles of key tile 0
-        ok = wait_slot(g);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        issue_s(0, g % SL);
-        if (w.n_b > 0) issue_s(1, g % SL);
-        commit(&slot_empty[g % SL]);
-        if (w.n_all == 1) commit(q_empty);
-        for (int j = 0; j < w.n_all; ++j) {
-          const uint32_t vi = g + 2 * j + 1;  // V_j
-          const uint32_t ki = vi + 1;         // K_{j+1}
-          ok = wait_slot(vi);
+      if constexpr (C::SEP_P) {
+        // S_X(t) may overwrite S_X once the softmax has read S_X(t-1)
+        uint32_t ns_iss[2] = {0, 0};
+        auto issue_s_sep = [&](int x, uint32_t kslot) {
+          if (ns_iss[x] > 0 && !wait_bar(&s_free[x], (ns_iss[x] - 1) & 1, kSiteMmaSFree))
+            return false;
+          ptx::tc_fence_after();
+          issue_s(x, kslot);
+          ++ns_iss[x];
+          return true;
+        };
+        auto issue_pv_sep = [&](int x, uint32_t vslot, bool first) {
+          const uint64_t vd = desc_v0 + ((vslot * C::TILE_BYTES) >> 4);
+          const uint32_t d_o = tmem + col_o<D>(x);
+          const uint32_t a_p = tmem + col_p(x);
+          const uint32_t acc0 = first ? 0u : 1u;
+          if (ptx::elect_one_sync()) {
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              ptx::mma_f16_ts(d_o, a_p + kk * 8, vd + ((kk * 16 * 128) >> 4), idO,
+                              kk > 0 ? 1u : acc0);
+            ptx::mma_commit(&pv_done[x]);
+          }
+          __syncwarp();
+        };
+        for (int r = 0; ok && r * G < U; ++r) {
+          const int u = unit_of_round(r, bid, G);
+          if (u >= U) continue;
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
+          ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
+          ++nq;
           if (!ok) break;
-          if (j < w.n_a) {
-            ok = wait_p(0, j == 0);
+          ok = wait_slot(g);  // K_0
+          if (!ok) break;
+          ptx::tc_fence_after();
+          ok = issue_s_sep(0, g % SL);
+          if (ok && w.n_b > 0) ok = issue_s_sep(1, g % SL);
+          if (!ok) break;
+          commit(&slot_empty[g % SL]);
+          if (w.n_all == 1) commit(q_empty);
+          for (int j = 0; j < w.n_all; ++j) {
+            const uint32_t vi = g + 2 * j + 1;  // V_j
+            const uint32_t ki = vi + 1;         // K_{j+1}
+            if (j + 1 < w.n_all) {
+              // scores of the next key tile first: they only need the
+              // softmax to have read this tile's scores
+              ok = wait_slot(ki);
+              if (!ok) break;
+              ptx::tc_fence_after();
+              if (j + 1 < w.n_a) ok = issue_s_sep(0, ki % SL);
+              if (ok && j + 1 < w.n_b) ok = issue_s_sep(1, ki % SL);
+              if (!ok) break;
+              commit(&slot_empty[ki % SL]);
+              if (j + 2 == w.n_all) commit(q_empty);
+            }
+            ok = wait_slot(vi);
             if (!ok) break;
-            issue_pv(0, vi % SL, j == 0);
-            if (j == w.n_a - 1) commit(&o_full[0]);
+            if (j < w.n_a) {
+              ok = wait_p(0, j == 0);
+              if (!ok) break;
+              issue_pv_sep(0, vi % SL, j == 0);
+              if (j == w.n_a - 1) commit(&o_full[0]);
+            }
+            if (j < w.n_b) {
+              ok = wait_p(1, j == 0);
+              if (!ok) break;
+              issue_pv_sep(1, vi % SL, j == 0);
+              if (j == w.n_b - 1) commit(&o_full[1]);
+            }
+            commit(&slot_empty[vi % SL]);
           }
-          if (j + 1 < w.n_all) {
-            ok = wait_slot(ki);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            if (j + 1 < w.n_a) issue_s(0, ki % SL);
-          }
-          if (j < w.n_b) {
-            ok = wait_p(1, j == 0);
-            if (!ok) break;
-            issue_pv(1, vi % SL, j == 0);
-            if (j == w.n_b - 1) commit(&o_full[1]);
-          }
-          commit(&slot_empty[vi % SL]);
-          if (j + 1 < w.n_all) {
-            if (j + 1 < w.n_b) issue_s(1, ki % SL);
-            commit(&slot_empty[ki % SL]);
-            if (j + 2 == w.n_all) commit(q_empty);
-          }
+          g += 2 * w.n_all;
         }
-        g += 2 * w.n_all;
+      } else {
+        for (int r = 0; ok && r * G < U; ++r) {
+          const int u = unit_of_round(r, bid, G);
+          if (u >= U) continue;
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
+          ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
+          ++nq;
+          if (!ok) break;
+          // prologue: both score tiles of key tile 0
+          ok = wait_slot(g);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_s(0, g % SL);
+          if (w.n_b > 0) issue_s(1, g % SL);
+          commit(&slot_empty[g % SL]);
+          if (w.n_all == 1) commit(q_empty);
+          for (int j = 0; j < w.n_all; ++j) {
+            const uint32_t vi = g + 2 * j + 1;  // V_j
+            const uint32_t ki = vi + 1;         // K_{j+1}
+            ok = wait_slot(vi);
+            if (!ok) break;
+            if (j < w.n_a) {
+              ok = wait_p(0, j == 0);
+              if (!ok) break;
+              issue_pv(0, vi % SL, j == 0);
+              if (j == w.n_a - 1) commit(&o_full[0]);
+            }
+            if (j + 1 < w.n_all) {
+              ok = wait_slot(ki);
+              if (!ok) break;
+              ptx::tc_fence_after();
+              if (j + 1 < w.n_a) issue_s(0, ki % SL);
+            }
+            if (j < w.n_b) {
+              ok = wait_p(1, j == 0);
+              if (!ok) break;
+              issue_pv(1, vi % SL, j == 0);
+              if (j == w.n_b - 1) commit(&o_full[1]);
+            }
+            commit(&slot_empty[vi % SL]);
+            if (j + 1 < w.n_all) {
+              if (j + 1 < w.n_b) issue_s(1, ki % SL);
+              commit(&slot_empty[ki % SL]);
+              if (j + 2 == w.n_all) commit(q_empty);
+            }
+          }
+          g += 2 * w.n_all;
+        }
       }
       // All MMAs this warp issued must be complete before TMEM is freed.
       commit(mma_done);
@@ -459,7 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t t_s = t_lane + col_s(x);
     const uint32_t t_o = t_lane + col_o<D>(x);
+    // where P_X goes: its own columns (SEP_P) or over S_X
+    const uint32_t t_p = C::SEP_P ? t_lane + col_p(x) : t_s;
     uint32_t ns = 0, no = 0;
+    uint32_t nps = 0;  // P_X tiles stored so far (SEP_P: PV_X(nps - 1) must finish first)
     bool ok = true;
 
     for (int rr = 0; ok && rr * G < U; ++rr) {
@@ -483,6 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         uint32_t sr[128];
         tmem_ld_row128(t_s, sr);
+        if constexpr (C::SEP_P) {
+          // the scores are in registers: S_X may be overwritten
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&s_free[x]);
+        }
         float* s = reinterpret_cast<float*>(sr);
 
         const int key0 = j * kBN;
@@ -532,11 +629,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
         l += rsa.x + rsa.y;
 
+        if constexpr (C::SEP_P) {
+          // P_X and O_X are free once the previous product PV_X finished
+          if (nps > 0) {
+            ok = ptx::mbar_wait(&pv_done[x], (nps - 1) & 1, status,
+                                status_word(kKernPrefill, kSiteSoftPv));
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+          }
+        }
         if (__any_sync(0xffffffffu, rescale)) {
           // O_X holds the sum through key tile j-1 (that product is complete:
-          // it was issued before S_X(j), whose completion this warp waited
-          // for). Multiply this warp's rows by their alpha in place; rows
-          // that keep their reference max multiply by 1.
+          // without SEP_P it was issued before S_X(j), whose completion this
+          // warp waited for; with SEP_P this warp waited for it just above).
+          // Multiply this warp's rows by their alpha in place; rows that keep
+          // their reference max multiply by 1.
           const float mul = rescale ? alpha : 1.f;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -548,12 +656,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st_32x32b_x32(t_o + c * 32, raw);
           }
         }
-        // P_X (16-bit pairs) into the first 64 columns of S_X
-        ptx::tmem_st_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        ptx::tmem_st_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        // P_X (16-bit pairs) into its columns (or the first 64 of S_X)
+        ptx::tmem_st_32x32b_x32(t_p, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        ptx::tmem_st_32x32b_x32(t_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&p_full[x]);
+        ++nps;
       }
       if (!ok) break;
 
