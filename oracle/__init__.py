@@ -11,6 +11,7 @@ from .oracle import (  # noqa: F401
     merge_partials,
     online_attention,
     online_softmax_states,
+    paged_decode_attention,
     split_kv_attention,
     split_partials,
     standard_attention,

@@ -24,6 +24,13 @@ Pages followed (cited by page title and section):
   section "What is being computed": per head Q is T_q x d, K and V are
   T_kv x d, over B sequences and h heads; causal: position i sees keys up to
   and including itself.
+* Paged KV cache: "Attention and Its Computational Cost", section "The other
+  shape: one query, many keys" names paging of the cache (with batching,
+  grouped-query attention and quantisation) among the ways serving systems
+  manage its size, without a layout. The oracle takes the plainest reading:
+  a sequence's cache is the concatenation of the pages its block table
+  lists, cut at its length; decode attends over exactly those keys
+  (paged_decode_attention).
 * Backward pass: "IO-Aware Attention: Tiling the Score Matrix Without
   Materializing It", section "What has to stay in fast memory" says only that
   the backward pass recomputes the softmax output from the saved Q, K, V and
@@ -64,6 +71,7 @@ __all__ = [
     "gqa_attention",
     "attention_backward",
     "gqa_attention_backward",
+    "paged_decode_attention",
 ]
 
 
@@ -382,3 +390,56 @@ def gqa_attention_backward(q, k, v, do, scale=None, causal=False):
         dk[:, j] += dki
         dv[:, j] += dvi
     return dq, dk, dv
+
+
+def paged_decode_attention(q, k_pages, v_pages, block_table, seq_lens, scale=None):
+    """Decode (one query row per sequence and head) against a paged cache,
+    float64: returns (O [B, h_q, d], lse [B, h_q]).
+
+    q: [B, h_q, d]; k_pages, v_pages: [num_pages, h_kv, page_size, d] (a
+    pool of fixed-size pages, each holding page_size consecutive cache rows
+    of every key/value head); block_table: [B, max_pages] page indices;
+    seq_lens: [B] cache lengths. Sequence b's keys are rows 0..n_b-1 of the
+    concatenation of pages block_table[b, 0], block_table[b, 1], ... (for
+    the heads), and query head i reads key/value head i // (h_q // h_kv).
+    Each row is then plain attention of one query against those keys
+    (standard_attention_row). A sequence of length 0 has no keys: its
+    output is 0 and its lse is -inf (the softmax over nothing has no value;
+    this is the oracle's convention, matched by the kernels).
+
+    The pages name paging among the cache-management techniques of serving
+    ("Attention and Its Computational Cost", section "The other shape: one
+    query, many keys") without a layout; this gather is the plainest reading.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    kp = np.asarray(k_pages, dtype=np.float64)
+    vp = np.asarray(v_pages, dtype=np.float64)
+    table = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    if q.ndim != 3 or kp.ndim != 4 or vp.shape != kp.shape:
+        raise ValueError("q must be [B, h_q, d] and the page pools [num_pages, h_kv, page_size, d]")
+    B, h_q, d = q.shape
+    num_pages, h_kv, page_size, dk = kp.shape
+    if dk != d or h_kv < 1 or h_q % h_kv != 0:
+        raise ValueError("head width or grouping mismatch")
+    if table.ndim != 2 or table.shape[0] != B or lens.shape != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
+    if (lens < 0).any() or (lens > table.shape[1] * page_size).any():
+        raise ValueError("a length exceeds the pages its block table can hold")
+    group = h_q // h_kv
+    out = np.zeros((B, h_q, d), dtype=np.float64)
+    lse = np.full((B, h_q), -np.inf, dtype=np.float64)
+    for b in range(B):
+        n = int(lens[b])
+        if n == 0:
+            continue
+        n_pages = -(-n // page_size)
+        pages = table[b, :n_pages]
+        if (pages < 0).any() or (pages >= num_pages).any():
+            raise ValueError("block table entry outside the page pool")
+        for i in range(h_q):
+            j = i // group
+            keys = np.concatenate([kp[p, j] for p in pages], axis=0)[:n]
+            vals = np.concatenate([vp[p, j] for p in pages], axis=0)[:n]
+            out[b, i], lse[b, i] = standard_attention_row(q[b, i], keys, vals, scale=scale)
+    return out, lse

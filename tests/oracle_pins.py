@@ -45,6 +45,7 @@ def real_oracle():
         gqa_attention=oracle.gqa_attention,
         attention_backward=oracle.attention_backward,
         gqa_attention_backward=oracle.gqa_attention_backward,
+        paged_decode_attention=oracle.paged_decode_attention,
     )
 
 
@@ -457,6 +458,74 @@ def check_backward_gqa(impl):
     return fails
 
 
+def _scatter_into_pages(k, v, lens, page_size, rng, spare=3):
+    """Lay contiguous per-sequence caches k, v [B, h_kv, T, d] out in a pool
+    of pages in random order; returns (k_pages, v_pages, block_table). Rows
+    past a sequence's length are left as garbage (must not be read)."""
+    B, h_kv, T, d = k.shape
+    max_pages = -(-T // page_size)
+    num_pages = B * max_pages + spare
+    perm = rng.permutation(num_pages)
+    kp = rng.standard_normal((num_pages, h_kv, page_size, d)) * 50.0   # garbage
+    vp = rng.standard_normal((num_pages, h_kv, page_size, d)) * 50.0
+    table = np.full((B, max_pages), -1, dtype=np.int64)
+    n = 0
+    for b in range(B):
+        for j in range(-(-int(lens[b]) // page_size)):
+            pg = int(perm[n])
+            n += 1
+            table[b, j] = pg
+            rows = slice(j * page_size, min((j + 1) * page_size, int(lens[b])))
+            cnt = rows.stop - rows.start
+            kp[pg, :, :cnt] = k[b, :, rows]
+            vp[pg, :, :cnt] = v[b, :, rows]
+    table[table < 0] = int(perm[-1])   # unused entries point at a valid page
+    return kp, vp, table
+
+
+def check_paged(impl):
+    import torch
+    import torch.nn.functional as F
+    fails = []
+    rng = _rng(13)
+    for (B, h_q, h_kv, T, d, page_size) in ((3, 4, 2, 37, 8, 8), (2, 3, 3, 64, 16, 16), (4, 8, 1, 20, 4, 4)):
+        k = rng.standard_normal((B, h_kv, T, d))
+        v = rng.standard_normal((B, h_kv, T, d))
+        q = rng.standard_normal((B, h_q, d))
+        lens = rng.integers(1, T + 1, size=B)
+        lens[0] = T
+        kp, vp, table = _scatter_into_pages(k, v, lens, page_size, rng)
+        o, lse = impl.paged_decode_attention(q, kp, vp, table, lens)
+        g = h_q // h_kv
+        for b in range(B):
+            n = int(lens[b])
+            o_ref, l_ref = impl.gqa_attention(q[b:b + 1, :, None, :], k[b:b + 1, :, :n], v[b:b + 1, :, :n])
+            if not (_close(o[b], o_ref[0, :, 0]) and _close(lse[b], l_ref[0, :, 0])):
+                fails.append(f"paged vs contiguous b={b} shape={(B, h_q, h_kv, T, d, page_size)}")
+            kk = torch.from_numpy(np.repeat(k[b:b + 1, :, :n], g, axis=1))
+            vv = torch.from_numpy(np.repeat(v[b:b + 1, :, :n], g, axis=1))
+            o_lib = F.scaled_dot_product_attention(torch.from_numpy(q[b:b + 1, :, None, :]), kk, vv)
+            if not _close(o[b], o_lib.numpy()[0, :, 0], rtol=1e-10, atol=1e-12):
+                fails.append(f"paged vs library b={b}")
+        # renumbering the pages (and the table with them) changes nothing
+        perm = rng.permutation(kp.shape[0])
+        inv = np.argsort(perm)
+        o2, lse2 = impl.paged_decode_attention(q, kp[perm], vp[perm], inv[table], lens)
+        if not (_close(o2, o) and _close(lse2, lse)):
+            fails.append("page renumbering must not change the result")
+    # a zero length: output 0, lse -inf, other rows unaffected
+    k = rng.standard_normal((2, 1, 9, 4))
+    v = rng.standard_normal((2, 1, 9, 4))
+    q = rng.standard_normal((2, 2, 4))
+    kp, vp, table = _scatter_into_pages(k, v, np.array([9, 9]), 4, rng)
+    o, lse = impl.paged_decode_attention(q, kp, vp, table, np.array([0, 9]))
+    o_full, lse_full = impl.paged_decode_attention(q, kp, vp, table, np.array([9, 9]))
+    if not (np.all(o[0] == 0) and np.all(np.isneginf(lse[0])) and _close(o[1], o_full[1])
+            and _close(lse[1], lse_full[1])):
+        fails.append("zero-length sequence convention")
+    return fails
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_blockwise_equals_full,
@@ -471,6 +540,7 @@ ALL_CHECKS = [
     check_backward_closed_forms,
     check_backward_invariants,
     check_backward_gqa,
+    check_paged,
 ]
 
 

@@ -151,6 +151,29 @@ def _gqa_bwd_overwrites(q, k, v, do, scale=None, causal=False):
     return dq, dk, dv
 
 
+def _paged_factory(page_off=0, ignore_len=False, head_modulo=False):
+    def paged(q, k_pages, v_pages, block_table, seq_lens, scale=None):
+        q = np.asarray(q, dtype=np.float64)
+        kp = np.asarray(k_pages, dtype=np.float64)
+        vp = np.asarray(v_pages, dtype=np.float64)
+        B, h_q, d = q.shape
+        num_pages, h_kv, page_size, _ = kp.shape
+        out = np.zeros((B, h_q, d))
+        lse = np.full((B, h_q), -np.inf)
+        for b in range(B):
+            n = int(seq_lens[b]) if not ignore_len else block_table.shape[1] * page_size
+            if n == 0:
+                continue
+            pages = [(int(p) + page_off) % num_pages for p in block_table[b, :-(-n // page_size)]]
+            for i in range(h_q):
+                j = (i % h_kv) if head_modulo else i // (h_q // h_kv)
+                keys = np.concatenate([kp[p, j] for p in pages])[:n]
+                vals = np.concatenate([vp[p, j] for p in pages])[:n]
+                out[b, i], lse[b, i] = oracle.standard_attention_row(q[b, i], keys, vals, scale=scale)
+        return out, lse
+    return paged
+
+
 MUTANTS = {
     "online_drops_rescale": _with(online_attention=_online_factory(rescale=False)),
     "online_rescale_wrong_sign": _with(online_attention=_online_factory(sign=-1.0)),
@@ -172,6 +195,9 @@ MUTANTS = {
     "backward_dv_unnormalised_p": _with(attention_backward=_bwd_factory(dv_unnormalised=True)),
     "backward_causal_excludes_diagonal": _with(attention_backward=_bwd_factory(causal_off=-1)),
     "gqa_backward_overwrites": _with(gqa_attention_backward=_gqa_bwd_overwrites),
+    "paged_off_by_one_page": _with(paged_decode_attention=_paged_factory(page_off=1)),
+    "paged_ignores_length": _with(paged_decode_attention=_paged_factory(ignore_len=True)),
+    "paged_modulo_head_mapping": _with(paged_decode_attention=_paged_factory(head_modulo=True)),
 }
 
 
