@@ -443,6 +443,37 @@ def run_kernel_case(args):
     else:
         def call():
             _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+    paged_bytes = None
+    if args.page_size:
+        # the decode workload's cache laid out in pages, in a seeded random
+        # order; lengths full, or (--var-len) uniform in [T/4, T]
+        if w.T_q != 1:
+            raise SystemExit("--page-size needs a decode workload (T_q = 1)")
+        ps = args.page_size
+        gen = torch.Generator().manual_seed(w.seed + 11)
+        lens = torch.full((w.B,), w.T_kv, dtype=torch.int32)
+        if args.var_len:
+            lens = torch.randint(w.T_kv // 4, w.T_kv + 1, (w.B,), generator=gen, dtype=torch.int32)
+        max_pages = -(-w.T_kv // ps)
+        num_pages = w.B * max_pages
+        perm = torch.randperm(num_pages, generator=gen)
+        table = perm.reshape(w.B, max_pages).to(torch.int32)
+        kp = torch.empty((num_pages, w.kv_heads, ps, w.d), dtype=k.dtype, device=k.device)
+        vp = torch.empty_like(kp)
+        pages_of = k.view(w.B, w.kv_heads, max_pages, ps, w.d).permute(0, 2, 1, 3, 4)
+        kp[table.long().flatten().to(k.device)] = pages_of.reshape(num_pages, w.kv_heads, ps, w.d)
+        pages_of = v.view(w.B, w.kv_heads, max_pages, ps, w.d).permute(0, 2, 1, 3, 4)
+        vp[table.long().flatten().to(k.device)] = pages_of.reshape(num_pages, w.kv_heads, ps, w.d)
+        del k, v
+        qd = q[:, :, 0].contiguous()
+        od = torch.empty_like(qd)
+        lsed = torch.empty((w.B, w.h), dtype=torch.float32, device=q.device)
+        table_d, lens_d = table.to(q.device), lens.to(q.device)
+        paged_bytes = (2 * int(lens.sum()) * w.kv_heads * w.d * 2 + 2 * w.B * w.h * w.d * 2
+                       + w.B * w.h * 4)
+
+        def call():
+            _lib.attn_fwd_paged_decode(qd, kp, vp, table_d, lens_d, out=od, lse=lsed)
     if args.backward:
         from exact_io_aware_attn_gb300.inputs import make_dout
         call()
@@ -470,11 +501,17 @@ def run_kernel_case(args):
     if args.backward:
         fl = cost.bwd_flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
         by = cost.bwd_min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d, h_kv=w.kv_heads)
+    elif paged_bytes is not None:
+        fl = cost.flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
+        by = paged_bytes
     else:
         fl = cost.flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
         by = cost.min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d, h_kv=w.kv_heads)
     peaks = load_peaks()
-    print(json.dumps({"workload": w.name, "pass": "backward" if args.backward else "forward",
+    kind = "backward" if args.backward else (
+        f"paged decode, page {args.page_size}" + (", variable lengths" if args.var_len else "")
+        if args.page_size else "forward")
+    print(json.dumps({"workload": w.name, "pass": kind,
                       "B": w.B, "kernel": _lib.last_kernel_name(),
                       "us_per_call": sec * 1e6, "tflops": fl / sec / 1e12,
                       "gbs": by / sec / 1e9,
@@ -496,6 +533,11 @@ def main(argv=None):
                     help="batch size override for --kernel-case")
     ap.add_argument("--backward", action="store_true",
                     help="with --kernel-case: time the backward pass (attn_bwd) instead")
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="with a decode --kernel-case: lay the cache out in pages of this many "
+                         "rows (random page order) and time attn_fwd_paged_decode")
+    ap.add_argument("--var-len", action="store_true",
+                    help="with --page-size: sequence lengths uniform in [T/4, T]")
     args = ap.parse_args(argv)
     if args.kernel_case:
         return run_kernel_case(args)

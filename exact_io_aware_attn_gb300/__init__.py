@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     attn_fwd,
     attn_fwd_decode_noalloc,
     attn_fwd_gqa,
+    attn_fwd_paged_decode,
     decode_num_splits,
     fwd_raw,
     get_device_error,

@@ -46,6 +46,9 @@ SIGNATURES = {
     "attn_bwd_gqa": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F,
                           _I, _I, _VP, _SZ, _VP]),
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "attn_fwd_paged_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
+                                   _F, _I, _I, _VP, _SZ, _VP]),
+    "attn_paged_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
 }
 
 # Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
@@ -336,3 +339,58 @@ def attn_bwd(q, k, v, o, lse, dout, *, scale=None, causal=False, dq=None, dk=Non
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+def paged_workspace_bytes(B, h_q, d, page_size, max_pages_per_seq, num_splits=0) -> int:
+    return int(lib().attn_paged_workspace_bytes(B, h_q, d, page_size, max_pages_per_seq,
+                                                num_splits))
+
+
+def paged_decode_raw(q_ptr, kp_ptr, vp_ptr, table_ptr, lens_ptr, o_ptr, lse_ptr, B, h_q, h_kv, d,
+                     page_size, max_pages, num_pages, scale, dtype, num_splits=0,
+                     workspace_ptr=None, workspace_nbytes=0, stream_ptr=None) -> int:
+    """Direct call of attn_fwd_paged_decode; returns the status code."""
+    return int(lib().attn_fwd_paged_decode(q_ptr, kp_ptr, vp_ptr, table_ptr, lens_ptr, o_ptr,
+                                           lse_ptr, B, h_q, h_kv, d, page_size, max_pages,
+                                           num_pages, float(scale), int(dtype), int(num_splits),
+                                           workspace_ptr, int(workspace_nbytes), stream_ptr))
+
+
+def attn_fwd_paged_decode(q, k_pages, v_pages, block_table, seq_lens, *, scale=None, out=None,
+                          lse=None, num_splits=0, workspace=None, stream=None):
+    """Decode against a paged cache. q: [B, h_q, d] (or [B, h_q, 1, d]);
+    k_pages, v_pages: [num_pages, h_kv, page_size, d]; block_table: int32
+    [B, max_pages]; seq_lens: int32 [B]; all contiguous CUDA tensors.
+    Returns (o like q, lse [B, h_q] fp32)."""
+    import torch
+    for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
+                    ("block_table", block_table), ("seq_lens", seq_lens)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages must be [num_pages, h_kv, page_size, d]")
+    if not (q.dtype == k_pages.dtype == v_pages.dtype):
+        raise TypeError("q and the page pools must share one dtype")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    num_pages, h_kv, page_size, d = k_pages.shape
+    B, h_q = q.shape[0], q.shape[1]
+    if q.shape[-1] != d or q.numel() != B * h_q * d:
+        raise ValueError("q must be [B, h_q, d] or [B, h_q, 1, d]")
+    if block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, h_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with torch.cuda.device(q.device):
+        st = paged_decode_raw(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                              block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, h_q, h_kv, d, page_size, block_table.shape[1],
+                              num_pages, scale, _dtype_code(q), num_splits, wp, wn,
+                              _stream_ptr(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_paged_decode")
+    return out, lse

@@ -5,6 +5,7 @@
 // nothing here computes attention.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -142,7 +143,11 @@ attn_status_t validate(const void* q, const void* k, const void* v, void* o, flo
 // and of the bandwidth bound; a last wave a few percent full costs ~10%.
 // `rows` = split CTAs per partition index (B * h for plain attention).
 int choose_splits(long long rows, int T_kv, int d, int heads_per_cta) {
-  const long long cap = static_cast<long long>(sm_count()) * split_ctas_per_sm(d, heads_per_cta);
+  return choose_splits_cap(rows, T_kv,
+                           static_cast<long long>(sm_count()) * split_ctas_per_sm(d, heads_per_cta));
+}
+
+int choose_splits_cap(long long rows, int T_kv, long long cap) {
   const long long max_s = std::max(1ll, std::min<long long>(kMaxSplits, T_kv / 128));
   const long long target = std::min(max_s, std::max(1ll, (8 * cap + rows / 2) / rows));
   const long long lo = std::max(1ll, (target * 3) / 4);
@@ -298,6 +303,91 @@ attn_status_t run_bwd(const void* q, const void* k, const void* v, const void* o
   return ATTN_OK;
 }
 
+
+int paged_ctas_per_sm(int d) {
+  static std::mutex mu;
+  static int cache[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  std::lock_guard<std::mutex> g(mu);
+  int& c = cache[dev][d == 128];
+  if (!c) c = attn::decode_paged_ctas_per_sm(d);
+  return c;
+}
+
+// Paged decode: the split count for a shape, from the longest cache the
+// block table can name (the lengths live on the device).
+int paged_auto_splits(int B, int h_q, int d, int page_size, int max_pages) {
+  const long long cap = static_cast<long long>(sm_count()) * paged_ctas_per_sm(d);
+  const long long t = std::min<long long>(0x7fffffffll, static_cast<long long>(page_size) * max_pages);
+  return attn::detail::choose_splits_cap(static_cast<long long>(B) * h_q, static_cast<int>(t), cap);
+}
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+attn_status_t run_paged(const void* q, const void* k_pages, const void* v_pages,
+                        const int* block_table, const int* seq_lens, void* o, float* lse, int B,
+                        int h_q, int h_kv, int d, int page_size, int max_pages, int num_pages,
+                        float scale, int dtype, int num_splits, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (B < 0 || h_q < 0 || h_kv < 1 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (h_q % h_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!pow2(page_size) || page_size > 65536 || max_pages < 1 || num_pages < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(page_size) * max_pages > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * h_q;
+  if (BH == 0) {
+    t_last_kernel = "none";
+    return ATTN_OK;
+  }
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o || !lse)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(o, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const int splits = num_splits > 0 ? num_splits : paged_auto_splits(B, h_q, d, page_size, max_pages);
+  if (BH * splits > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  const size_t qo = static_cast<size_t>(BH) * d * 2;
+  const size_t pool = static_cast<size_t>(num_pages) * h_kv * page_size * d * 2;
+  const size_t tab = static_cast<size_t>(B) * max_pages * 4;
+  const size_t lens = static_cast<size_t>(B) * 4;
+  const size_t lse_b = static_cast<size_t>(BH) * 4;
+  struct Buf { const void* p; size_t n; };
+  const Buf ins[] = {{q, qo}, {k_pages, pool}, {v_pages, pool}, {block_table, tab}, {seq_lens, lens}};
+  for (const Buf& b : ins)
+    if (overlaps(o, qo, b.p, b.n) || overlaps(lse, lse_b, b.p, b.n)) return ATTN_ERR_INVALID_ARG;
+  if (overlaps(o, qo, lse, lse_b)) return ATTN_ERR_INVALID_ARG;
+  const size_t need = ws_bytes(B, h_q, d, splits);
+  const bool own = workspace == nullptr && workspace_bytes == 0;
+  if (!own) {
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ATTN_ERR_WORKSPACE;
+    for (const Buf& b : ins)
+      if (overlaps(workspace, need, b.p, b.n)) return ATTN_ERR_WORKSPACE;
+    if (overlaps(workspace, need, o, qo) || overlaps(workspace, need, lse, lse_b))
+      return ATTN_ERR_WORKSPACE;
+  }
+  int shift = 0;
+  while ((1 << shift) < page_size) ++shift;
+  attn::PagedProblem p{q, k_pages, v_pages, block_table, seq_lens, o, lse, B, h_q, h_kv, d, shift,
+                       max_pages, num_pages, scale, dtype == ATTN_BF16 ? 1 : 0, status_ptr()};
+  if (!p.status) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  if (own) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), need, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  const char* name = "none";
+  const cudaError_t e = attn::launch_decode_paged(p, splits, ws, s, &name);
+  if (own) cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  t_last_kernel = name;
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -362,6 +452,28 @@ attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const vo
                  dtype, workspace, workspace_bytes, stream);
 }
 
+attn_status_t attn_fwd_paged_decode(const void* q, const void* k_pages, const void* v_pages,
+                                    const int* block_table, const int* seq_lens, void* o,
+                                    float* lse, int B, int h_q, int h_kv, int d, int page_size,
+                                    int max_pages_per_seq, int num_pages, float scale, int dtype,
+                                    int num_splits, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  return run_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, h_q, h_kv, d, page_size,
+                   max_pages_per_seq, num_pages, scale, dtype, num_splits, workspace,
+                   workspace_bytes, stream);
+}
+
+size_t attn_paged_workspace_bytes(int B, int h_q, int d, int page_size, int max_pages_per_seq,
+                                  int num_splits) {
+  if (B < 1 || h_q < 1 || (d != 64 && d != 128) || !pow2(page_size) || page_size > 65536 ||
+      max_pages_per_seq < 1 || num_splits < 0 || num_splits > kMaxSplits)
+    return 0;
+  if (static_cast<long long>(page_size) * max_pages_per_seq > 0x7fffffffll) return 0;
+  const int splits =
+      num_splits > 0 ? num_splits : paged_auto_splits(B, h_q, d, page_size, max_pages_per_seq);
+  return ws_bytes(B, h_q, d, splits);
+}
+
 size_t attn_bwd_workspace_bytes(int B, int h, int T_q, int T_kv, int d) {
   if (B < 1 || h < 1 || T_q < 1 || T_kv < 1 || (d != 64 && d != 128)) return 0;
   return attn::bwd_workspace_floats(static_cast<long long>(B) * h, T_q) * sizeof(float);
@@ -387,7 +499,9 @@ attn_status_t attn_get_device_error(void* stream, unsigned int* site) {
   if (site) *site = word;
   if (word == 0) return ATTN_OK;
   const unsigned int code = word & 0xffu;
-  return code == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA;
+  if (code == ATTN_ERR_TIMEOUT) return ATTN_ERR_TIMEOUT;
+  if (code == ATTN_ERR_INVALID_ARG) return ATTN_ERR_INVALID_ARG;  // found on the device
+  return ATTN_ERR_CUDA;
 }
 
 const char* attn_status_string(int status) {

@@ -61,6 +61,29 @@ inline size_t bwd_workspace_floats(long long BH, int T_q) {
 
 cudaError_t launch_backward(const BwdProblem& p, cudaStream_t stream, const char** name);
 
+// Decode against a paged cache (attn_fwd_paged_decode): pages
+// [num_pages][h_kv][page_size][d], block_table [B][max_pages] int32,
+// seq_lens [B] int32 (device memory).
+struct PagedProblem {
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const int* block_table;
+  const int* seq_lens;
+  void* o;
+  float* lse;
+  int B, h_q, h_kv, d;
+  int page_shift;         // log2(page_size)
+  int max_pages, num_pages;
+  float scale;
+  int bf16;
+  unsigned int* status;
+};
+
+cudaError_t launch_decode_paged(const PagedProblem& p, int num_splits, float* ws,
+                                cudaStream_t stream, const char** name);
+int decode_paged_ctas_per_sm(int d);
+
 // Query heads one decode split CTA serves (all sharing one key/value head):
 // the largest of 8, 4, 2, 1 that divides the group size h / h_kv.
 inline int decode_heads_per_cta(int group) {
@@ -79,6 +102,8 @@ attn_status_t validate(const void* q, const void* k, const void* v, void* o, flo
 // Decode split count chosen by shape on the current device (attn_api.cu):
 // `rows` CTAs per partition index (B * h_kv * group / heads_per_cta).
 int choose_splits(long long rows, int T_kv, int d, int heads_per_cta);
+// The same rule for a given capacity (split CTAs resident on the device).
+int choose_splits_cap(long long rows, int T_kv, long long cap);
 }  // namespace detail
 
 // Floats per partial: d outputs, then running max and running sum, padded

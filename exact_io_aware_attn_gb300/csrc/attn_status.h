@@ -21,8 +21,15 @@ constexpr uint32_t kStatusTimeout = 4u;  // == ATTN_ERR_TIMEOUT
 
 enum KernelId : uint32_t {
   kKernPrefill = 1, kKernDecodeSplit = 2, kKernDecodeCombine = 3, kKernSelftest = 4,
-  kKernBwdKV = 5, kKernBwdQ = 6
+  kKernBwdKV = 5, kKernBwdQ = 6, kKernDecodePaged = 7
 };
+
+// A word for a status code other than a timeout (e.g. ATTN_ERR_INVALID_ARG
+// for a block-table entry outside the page pool, found on the device).
+__host__ __device__ constexpr uint32_t status_word_code(uint32_t code, uint32_t kernel,
+                                                        uint32_t site) {
+  return code | (kernel << 8) | (site << 16);
+}
 
 __host__ __device__ constexpr uint32_t status_word(uint32_t kernel, uint32_t site) {
   return kStatusTimeout | (kernel << 8) | (site << 16);

@@ -90,8 +90,12 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[N], f
 
 // One CTA: partition s of the keys of one query head (one query head per
 // CTA: plain attention, or a grouped-query group of odd size).
+// Occupancy: measured on GB300 (16K-key cache, 1.61 GB), 8 resident CTAs per
+// SM stream the cache ~7% faster than the 9 that 50 registers would allow
+// (230 vs 248 us at every split count tried); the bound lets the compiler
+// use up to 64 registers and so fixes 8.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 8)
     decode_split_1head_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,
                               const uint8_t* __restrict__ v, float* __restrict__ ws, int T_kv,
                               int S, int chunk, float scale_log2, int group) {
@@ -212,6 +216,147 @@ __global__ void __launch_bounds__(kDecThreads)
   // once every CTA has passed this point (or exited) it may be scheduled, and
   // it waits (griddepcontrol.wait) for this grid's completion and memory
   // flush before reading any partial.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// One CTA: partition s of the keys of one query head of one sequence, with
+// the cache in pages: key t of sequence b is row t % page_size of page
+// block_table[b][t / page_size]; a page holds page_size rows of every
+// key/value head ([num_pages][h_kv][page_size][d]). Each sequence has its
+// own length (seq_lens[b], clamped to the pages its table can name) and is
+// cut into S partitions of ceil(len / S) keys. A table entry outside the
+// pool is never dereferenced: the key is skipped and ATTN_ERR_INVALID_ARG is
+// recorded in the status word (first error wins).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_paged_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ kpg,
+                              const uint8_t* __restrict__ vpg, const int* __restrict__ table,
+                              const int* __restrict__ lens, float* __restrict__ ws, int S,
+                              float scale_log2, int h_q, int group, int h_kv, int page_shift,
+                              int max_pages, int num_pages, unsigned int* __restrict__ status) {
+  constexpr int TPK = D / 8;            // threads per key
+  constexpr int KPW = 32 / TPK;         // keys per warp per load
+  constexpr int SLOTS = (kDecThreads / 32) * KPW;
+  constexpr int ROW = D * 2;            // bytes per key row
+
+  const int s = static_cast<int>(blockIdx.x % static_cast<unsigned>(S));
+  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(S));  // b * h_q + head
+  const int b = bh / h_q;
+  const int kvh = (bh - b * h_q) / group;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % TPK;           // which 8 dims
+  const int slot = warp * KPW + lane / TPK;
+
+  const int len = max(0, min(__ldg(lens + b), max_pages << page_shift));
+  const int chunk = (len + S - 1) / S;
+  const int lo = min(s * chunk, len);
+  const int hi = min(lo + chunk, len);
+  const int* trow = table + static_cast<size_t>(b) * max_pages;
+  const int row_mask = (1 << page_shift) - 1;
+  // rows of one page across all heads, and this head's first row in a page
+  const size_t page_rows = static_cast<size_t>(h_kv) << page_shift;
+  const uint8_t* kbase = kpg + (static_cast<size_t>(kvh) << page_shift) * ROW + sub * 16;
+  const uint8_t* vbase = vpg + (static_cast<size_t>(kvh) << page_shift) * ROW + sub * 16;
+
+  float qf[8];
+  unpack8<BF16>(*reinterpret_cast<const uint4*>(q + static_cast<size_t>(bh) * ROW + sub * 16), qf);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
+
+  float m = -INFINITY, l = 0.f;
+  float o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = 0.f;
+
+  for (int base = lo; base < hi; base += SLOTS * kUnroll) {
+    uint4 kr[kUnroll], vr[kUnroll];
+    bool valid[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int key = base + u * SLOTS + slot;
+      valid[u] = key < hi;
+      kr[u] = make_uint4(0, 0, 0, 0);
+      vr[u] = make_uint4(0, 0, 0, 0);
+      if (valid[u]) {
+        const int pg = __ldg(trow + (key >> page_shift));
+        if (static_cast<unsigned>(pg) < static_cast<unsigned>(num_pages)) {
+          const size_t off = (static_cast<size_t>(pg) * page_rows + (key & row_mask)) * ROW;
+          kr[u] = ld_stream(kbase + off);
+          vr[u] = ld_stream(vbase + off);
+        } else {
+          valid[u] = false;
+          atomicCAS(status, 0u, status_word_code(1u /* ATTN_ERR_INVALID_ARG */, kKernDecodePaged, 1u));
+        }
+      }
+    }
+    float sc[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      float kf[8];
+      unpack8<BF16>(kr[u], kf);
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
+#pragma unroll
+      for (int w = 1; w < TPK; w <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
+      sc[u] = valid[u] ? dot : -INFINITY;
+    }
+    float mt = m;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) mt = fmaxf(mt, sc[u]);
+    const float ref = (mt == -INFINITY) ? 0.f : mt;
+    const float a = ex2f(m - ref);
+    l *= a;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] *= a;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const float p = ex2f(sc[u] - ref);
+      l += p;
+      float vf[8];
+      unpack8<BF16>(vr[u], vf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = fmaf(p, vf[i], o[i]);
+    }
+    m = mt;
+  }
+
+  // Merge the key slots of this warp (lanes with the same `sub`).
+#pragma unroll
+  for (int w = TPK; w < 32; w <<= 1) {
+    float o2[8];
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, w);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o2[i] = __shfl_xor_sync(0xffffffffu, o[i], w);
+    merge_state<8>(m, l, o, m2, l2, o2);
+  }
+  // Then the four warps.
+  __shared__ float sh_o[4][D];
+  __shared__ float sh_ml[4][2];
+  if (lane < TPK) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sh_o[warp][sub * 8 + i] = o[i];
+    if (lane == 0) {
+      sh_ml[warp][0] = m;
+      sh_ml[warp][1] = l;
+    }
+  }
+  __syncthreads();
+  if (warp == 0 && lane < TPK) {
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      float o2[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o2[i] = sh_o[w][sub * 8 + i];
+      merge_state<8>(m, l, o, sh_ml[w][0], sh_ml[w][1], o2);
+    }
+    float* part = ws + (static_cast<size_t>(bh) * S + s) * decode_partial_floats(D);
+    *reinterpret_cast<float4*>(part + sub * 8) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4*>(part + sub * 8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    if (lane == 0) *reinterpret_cast<float4*>(part + D) = make_float4(m, l, 0.f, 0.f);
+  }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -392,7 +537,7 @@ __global__ void __launch_bounds__(128)
   for (int s = lane; s < S; s += 32) M = fmaxf(M, part[s * stride + D]);
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
-  // every row has at least one key, so M is finite
+  // M is finite unless the row has no keys (paged path, length 0)
   float L = 0.f;
   float acc[PER];
 #pragma unroll
@@ -418,7 +563,9 @@ __global__ void __launch_bounds__(128)
   }
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) L += __shfl_xor_sync(0xffffffffu, L, w);
-  const float inv = 1.f / L;
+  // L = 0 only for a row with no keys at all (a zero-length sequence of the
+  // paged path): output 0 and lse -inf instead of 0/0
+  const float inv = L > 0.f ? 1.f / L : 0.f;
   uint8_t* orow = out + static_cast<size_t>(bh) * D * 2 + lane * PER * 2;
   if constexpr (PER == 2) {
     uint32_t w;
@@ -444,7 +591,7 @@ __global__ void __launch_bounds__(128)
     }
     *reinterpret_cast<uint2*>(orow) = make_uint2(w[0], w[1]);
   }
-  if (lane == 0) lse[bh] = (M + __log2f(L)) * 0.69314718055994531f;
+  if (lane == 0) lse[bh] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 template <int D, bool BF16, int G>
@@ -491,6 +638,31 @@ cudaError_t launch_g(const FwdProblem& p, int S, float* ws, cudaStream_t stream)
   }
 }
 
+template <int D, bool BF16>
+cudaError_t launch_paged_t(const PagedProblem& p, int S, float* ws, cudaStream_t stream) {
+  const int BH = p.B * p.h_q;
+  const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+  dim3 g1(static_cast<unsigned>(S) * static_cast<unsigned>(BH));
+  decode_paged_split_kernel<D, BF16><<<g1, kDecThreads, 0, stream>>>(
+      static_cast<const uint8_t*>(p.q), static_cast<const uint8_t*>(p.k_pages),
+      static_cast<const uint8_t*>(p.v_pages), p.block_table, p.seq_lens, ws, S, scale_log2, p.h_q,
+      p.h_q / p.h_kv, p.h_kv, p.page_shift, p.max_pages, p.num_pages, p.status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((BH + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>, static_cast<const float*>(ws),
+                            static_cast<uint8_t*>(p.o), p.lse, BH, S);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const FwdProblem& p, int num_splits, float* ws, cudaStream_t stream,
@@ -535,6 +707,37 @@ int decode_split_ctas_per_sm(int d, int heads_per_cta) {
       default: e = occ(decode_split_1head_kernel<128, true>); break;
     }
   }
+  return (e == cudaSuccess && n > 0) ? n : 8;
+}
+
+}  // namespace attn
+
+namespace attn {
+
+cudaError_t launch_decode_paged(const PagedProblem& p, int num_splits, float* ws,
+                                cudaStream_t stream, const char** name) {
+  cudaError_t e;
+  if (p.d == 64) {
+    e = p.bf16 ? launch_paged_t<64, true>(p, num_splits, ws, stream)
+               : launch_paged_t<64, false>(p, num_splits, ws, stream);
+    *name = p.bf16 ? "decode_paged_split_d64_bf16+decode_combine"
+                   : "decode_paged_split_d64_f16+decode_combine";
+  } else {
+    e = p.bf16 ? launch_paged_t<128, true>(p, num_splits, ws, stream)
+               : launch_paged_t<128, false>(p, num_splits, ws, stream);
+    *name = p.bf16 ? "decode_paged_split_d128_bf16+decode_combine"
+                   : "decode_paged_split_d128_f16+decode_combine";
+  }
+  return e;
+}
+
+int decode_paged_ctas_per_sm(int d) {
+  int n = 0;
+  const cudaError_t e =
+      d == 64 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_paged_split_kernel<64, true>,
+                                                              kDecThreads, 0)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_paged_split_kernel<128, true>,
+                                                              kDecThreads, 0);
   return (e == cudaSuccess && n > 0) ? n : 8;
 }
 

@@ -154,8 +154,10 @@ int attn_decode_num_splits(int B, int h, int T_kv, int d);
 /*
  * attn_get_device_error -- synchronises `stream`, then reads and clears the
  * current device's status word. Returns ATTN_OK if no kernel recorded an
- * error since the last read, ATTN_ERR_TIMEOUT if a bounded wait gave up, or
- * ATTN_ERR_CUDA if the synchronisation itself failed. If `site` is not NULL
+ * error since the last read, ATTN_ERR_TIMEOUT if a bounded wait gave up,
+ * ATTN_ERR_INVALID_ARG if a kernel found an invalid input in device memory
+ * (a paged-decode block-table entry outside the page pool), or ATTN_ERR_CUDA
+ * if the synchronisation itself failed. If `site` is not NULL
  * it receives the recorded word (0 if none): bits 0-7 the status code,
  * bits 8-15 the kernel, bits 16-23 the wait site.
  */
@@ -240,6 +242,51 @@ attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const vo
  * 8 * B * h_q * roundup(T_q, 128) bytes (0 for invalid or empty sizes).
  */
 size_t attn_bwd_workspace_bytes(int B, int h, int T_q, int T_kv, int d);
+
+/*
+ * attn_fwd_paged_decode -- decode (one query row per sequence and head)
+ * against a paged, variable-length KV cache, for batched serving.
+ *
+ * The cache lives in a pool of fixed-size pages: k_pages and v_pages are
+ * [num_pages][h_kv][page_size][d] in the 16-bit dtype (a page holds
+ * page_size consecutive cache rows of every key/value head, so one head's
+ * rows in a page are contiguous). Sequence b's keys are rows
+ * 0 .. seq_lens[b]-1 of the concatenation of pages block_table[b][0],
+ * block_table[b][1], ...; block_table is int32 [B][max_pages_per_seq] and
+ * seq_lens int32 [B], both in device memory (read by the kernel, never by
+ * the host). q and o are [B][h_q][d] (T_q = 1), lse fp32 [B][h_q]; query
+ * head i reads key/value head i / (h_q / h_kv). The pages name paging
+ * among the ways serving systems manage the cache ("Attention and Its
+ * Computational Cost", section "The other shape: one query, many keys");
+ * the layout is this library's.
+ *
+ * page_size: a power of two, 1..65536. A length above
+ * max_pages_per_seq * page_size is clamped to it; a length <= 0 gives
+ * o = 0 and lse = -inf for that sequence. A table entry outside
+ * [0, num_pages) is not dereferenced: its keys are skipped and the kernel
+ * records ATTN_ERR_INVALID_ARG in the device status word (read it with
+ * attn_get_device_error). Each sequence's keys are cut into num_splits
+ * partitions (0 = the library's choice from max_pages_per_seq * page_size)
+ * merged exactly as in attn_fwd's decode path. workspace: at least
+ * attn_paged_workspace_bytes(...) bytes, 16-byte aligned, or NULL with
+ * workspace_bytes 0 to have the library take it stream-ordered. Pointer
+ * rules: q, o and the page pools 16-byte aligned, block_table, seq_lens and
+ * lse 4-byte aligned; o and lse must not overlap any input or each other.
+ */
+attn_status_t attn_fwd_paged_decode(const void* q, const void* k_pages, const void* v_pages,
+                                    const int* block_table, const int* seq_lens, void* o,
+                                    float* lse, int B, int h_q, int h_kv, int d, int page_size,
+                                    int max_pages_per_seq, int num_pages, float scale, int dtype,
+                                    int num_splits, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
+ * attn_paged_workspace_bytes -- workspace attn_fwd_paged_decode needs:
+ * B*h_q*S*(d+4)*4 bytes, S = num_splits or the library's choice (0 for
+ * invalid sizes).
+ */
+size_t attn_paged_workspace_bytes(int B, int h_q, int d, int page_size, int max_pages_per_seq,
+                                  int num_splits);
 
 /*
  * attn_fwd_decode_noalloc -- the decode path (T_q == 1) without any

@@ -270,3 +270,56 @@ def test_backward_workspace_bytes(L):
     assert _lib.bwd_workspace_bytes(1, 1, 129, 129, 128) == 2 * 256 * 4
     assert _lib.bwd_workspace_bytes(1, 1, 100, 100, 96) == 0
     assert _lib.bwd_workspace_bytes(0, 1, 100, 100, 64) == 0
+
+
+# paged decode: fake addresses for the pools and tables
+KP, VP, TAB, LENS = (0x100000 * i for i in range(11, 15))
+
+
+def _paged(**over):
+    a = dict(B=2, h_q=4, h_kv=2, d=64, page_size=16, max_pages=8, num_pages=20, scale=0.125,
+             dtype=_lib.ATTN_BF16, num_splits=0)
+    ptrs = dict(q=Q, kp=KP, vp=VP, tab=TAB, lens=LENS, o=O, lse=LSE)
+    for key in list(over):
+        if key in ptrs:
+            ptrs[key] = over.pop(key)
+    ws, nbytes = over.pop("ws", None), over.pop("nbytes", 0)
+    a.update(over)
+    return _lib.paged_decode_raw(ptrs["q"], ptrs["kp"], ptrs["vp"], ptrs["tab"], ptrs["lens"],
+                                 ptrs["o"], ptrs["lse"], a["B"], a["h_q"], a["h_kv"], a["d"],
+                                 a["page_size"], a["max_pages"], a["num_pages"], a["scale"],
+                                 a["dtype"], a["num_splits"], ws, nbytes, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(kp=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(tab=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(lens=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(kp=KP + 8), _lib.ATTN_ERR_INVALID_ARG),          # misaligned pool
+    (dict(tab=TAB + 2), _lib.ATTN_ERR_INVALID_ARG),        # misaligned table
+    (dict(page_size=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=24), _lib.ATTN_ERR_INVALID_ARG),       # not a power of two
+    (dict(page_size=1 << 17), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(max_pages=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(num_pages=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(h_kv=3), _lib.ATTN_ERR_INVALID_ARG),             # 4 heads not a multiple of 3
+    (dict(h_kv=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(num_splits=1025), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(o=KP + 64), _lib.ATTN_ERR_INVALID_ARG),          # output overlaps the pool
+    (dict(lse=TAB), _lib.ATTN_ERR_INVALID_ARG),            # lse overlaps the table
+    (dict(ws=WS, nbytes=16, num_splits=8), _lib.ATTN_ERR_WORKSPACE),
+    (dict(ws=LENS, nbytes=1 << 20, num_splits=8), _lib.ATTN_ERR_WORKSPACE),
+    (dict(page_size=65536, max_pages=1 << 16), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(B=0), _lib.ATTN_OK),
+])
+def test_paged_decode_arguments(L, over, status):
+    assert _paged(**over) == status
+
+
+def test_paged_workspace_bytes(L):
+    assert _lib.paged_workspace_bytes(2, 4, 64, 16, 8, 5) == 2 * 4 * 5 * 68 * 4
+    assert _lib.paged_workspace_bytes(2, 4, 128, 16, 8, 3) == 2 * 4 * 3 * 132 * 4
+    assert _lib.paged_workspace_bytes(2, 4, 64, 24, 8, 5) == 0
+    assert _lib.paged_workspace_bytes(0, 4, 64, 16, 8, 5) == 0
