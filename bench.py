@@ -443,6 +443,15 @@ def run_kernel_case(args):
     else:
         def call():
             _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)
+    if args.splits is not None:
+        # prefill with an explicit key-partition count (1 = unsplit)
+        ws = torch.empty(max(16, _lib.splitkv_workspace_bytes(w.B, w.h, w.T_q, w.T_kv, w.d,
+                                                             args.splits)),
+                         dtype=torch.uint8, device=q.device)
+
+        def call():
+            _lib.attn_fwd_splitkv(q, k, v, causal=w.causal, out=o, lse=lse,
+                                  num_splits=args.splits, workspace=ws)
     paged_bytes = None
     if args.page_size:
         # the decode workload's cache laid out in pages, in a seeded random
@@ -536,6 +545,9 @@ def main(argv=None):
     ap.add_argument("--page-size", type=int, default=0,
                     help="with a decode --kernel-case: lay the cache out in pages of this many "
                          "rows (random page order) and time attn_fwd_paged_decode")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="with a prefill --kernel-case: attn_fwd_splitkv with this many key "
+                         "partitions (1 = unsplit; 0 = the library's choice)")
     ap.add_argument("--var-len", action="store_true",
                     help="with --page-size: sequence lengths uniform in [T/4, T]")
     args = ap.parse_args(argv)

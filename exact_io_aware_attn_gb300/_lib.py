@@ -49,6 +49,9 @@ SIGNATURES = {
     "attn_fwd_paged_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
                                    _F, _I, _I, _VP, _SZ, _VP]),
     "attn_paged_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_fwd_splitkv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP,
+                              _SZ, _VP]),
+    "attn_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
 }
 
 # Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
@@ -393,4 +396,42 @@ def attn_fwd_paged_decode(q, k_pages, v_pages, block_table, seq_lens, *, scale=N
                               _stream_ptr(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_paged_decode")
+    return out, lse
+
+
+def splitkv_workspace_bytes(B, h_q, T_q, T_kv, d, num_splits=0) -> int:
+    return int(lib().attn_splitkv_workspace_bytes(B, h_q, T_q, T_kv, d, num_splits))
+
+
+def splitkv_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h_q, h_kv, T_q, T_kv, d, scale, causal,
+                dtype, num_splits=0, workspace_ptr=None, workspace_nbytes=0, stream_ptr=None) -> int:
+    """Direct call of attn_fwd_splitkv; returns the status code."""
+    return int(lib().attn_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h_q, h_kv, T_q, T_kv,
+                                      d, float(scale), int(causal), int(dtype), int(num_splits),
+                                      workspace_ptr, int(workspace_nbytes), stream_ptr))
+
+
+def attn_fwd_splitkv(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_splits=0,
+                     workspace=None, stream=None):
+    """Prefill (T_q >= 2) with the key range cut into num_splits partitions
+    (0: the library's choice) and merged exactly. q [B, h_q, T_q, d]; k, v
+    [B, h_kv, T_kv, d]. Returns (o like q, lse [B, h_q, T_q] fp32)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    B, h_q, T_q, d = q.shape
+    h_kv, T_kv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, h_q, T_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with torch.cuda.device(q.device):
+        st = splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         B, h_q, h_kv, T_q, T_kv, d, scale, causal, _dtype_code(q), num_splits,
+                         wp, wn, _stream_ptr(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv")
     return out, lse

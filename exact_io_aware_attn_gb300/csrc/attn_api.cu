@@ -188,6 +188,62 @@ int auto_splits(int B, int h, int h_kv, int T_kv, int d) {
   return choose_splits(decode_rows(B, h, h_kv), T_kv, d, attn::decode_heads_per_cta(h / h_kv));
 }
 
+// Prefill key partitions: only when the (query-tile pair, head) units fill
+// less than half the SMs; then enough partitions to reach about one unit per
+// SM, at least 2 key tiles each, at most 64.
+int prefill_auto_splits(int B, int h, int T_q, int T_kv) {
+  const long long pairs = ((static_cast<long long>(T_q) + 127) / 128 + 1) / 2;
+  const long long units = pairs * B * h;
+  const long long sms = sm_count();
+  if (units * 2 > sms) return 1;
+  const long long n_kv = (static_cast<long long>(T_kv) + 127) / 128;
+  const long long s = std::min({(sms + units - 1) / units, n_kv / 2, 64ll});
+  return static_cast<int>(std::max(1ll, s));
+}
+
+size_t prefill_ws_bytes(int B, int h, int T_q, int d, int splits) {
+  return splits > 1 ? static_cast<size_t>(B) * h * T_q * splits * attn::decode_partial_floats(d) *
+                          sizeof(float)
+                    : 0;
+}
+
+// Prefill with `splits` key partitions (1: the plain kernel, no workspace).
+// Every argument check comes before the first CUDA call.
+attn_status_t run_prefill(attn::FwdProblem p, int splits, void* workspace, size_t workspace_bytes,
+                          bool own, cudaStream_t s) {
+  const char* name = "none";
+  if (splits <= 1) {
+    p.status = status_ptr();
+    if (!p.status) return ATTN_ERR_CUDA;
+    if (attn::launch_prefill(p, 1, nullptr, s, &name) != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_kernel = name;
+    return ATTN_OK;
+  }
+  const long long rows = static_cast<long long>(p.B) * p.h * p.T_q;
+  const long long pairs = ((static_cast<long long>(p.T_q) + 127) / 128 + 1) / 2;
+  if (rows > 0x7fffffffll || pairs * p.B * p.h * splits > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  const size_t need = prefill_ws_bytes(p.B, p.h, p.T_q, p.d, splits);
+  float* ws = static_cast<float*>(workspace);
+  if (!own) {
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ATTN_ERR_WORKSPACE;
+    const size_t qo = static_cast<size_t>(rows) * p.d * 2;
+    const size_t kv = static_cast<size_t>(p.B) * p.h_kv * p.T_kv * p.d * 2;
+    if (overlaps(workspace, need, p.q, qo) || overlaps(workspace, need, p.k, kv) ||
+        overlaps(workspace, need, p.v, kv) || overlaps(workspace, need, p.o, qo) ||
+        overlaps(workspace, need, p.lse, static_cast<size_t>(rows) * 4))
+      return ATTN_ERR_WORKSPACE;
+  }
+  p.status = status_ptr();
+  if (!p.status) return ATTN_ERR_CUDA;
+  if (own && cudaMallocAsync(reinterpret_cast<void**>(&ws), need, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const cudaError_t e = attn::launch_prefill(p, splits, ws, s, &name);
+  if (own) cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  t_last_kernel = name;
+  return ATTN_OK;
+}
+
 attn_status_t run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
                   int h_kv, int T_q, int T_kv, int d, float scale, int causal, int dtype,
                   int num_splits, void* workspace, size_t workspace_bytes, bool own_workspace,
@@ -206,11 +262,11 @@ attn_status_t run(const void* q, const void* k, const void* v, void* o, float* l
                      nullptr, h_kv};
   const char* name = "none";
   if (T_q > 1) {
-    p.status = status_ptr();
-    if (!p.status) return ATTN_ERR_CUDA;
-    if (attn::launch_prefill(p, s, &name) != cudaSuccess) return ATTN_ERR_CUDA;
-    t_last_kernel = name;
-    return ATTN_OK;
+    // attn_fwd (own workspace) cuts the key range of small problems into
+    // partitions; attn_fwd_ex and attn_fwd_gqa with a caller workspace keep
+    // the prefill unsplit (their workspace contract is decode-only)
+    const int splits = own_workspace ? prefill_auto_splits(B, h, T_q, T_kv) : 1;
+    return run_prefill(p, splits, nullptr, 0, true, s);
   }
   // the same choice attn_workspace_bytes(..., 0) reports (occupancy of the bf16
   // and fp16 split kernels is identical)
@@ -414,6 +470,35 @@ attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o,
   const bool own = workspace == nullptr && workspace_bytes == 0;
   return run(q, k, v, o, lse, B, h_q, h_kv, T_q, T_kv, d, scale, causal, dtype, num_splits,
              workspace, workspace_bytes, own, stream);
+}
+
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int h_q, int h_kv, int T_q, int T_kv, int d, float scale,
+                               int causal, int dtype, int num_splits, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (h_kv < 1) return ATTN_ERR_INVALID_ARG;
+  bool empty = false;
+  attn_status_t st = validate(q, k, v, o, lse, B, h_q, T_q, T_kv, d, scale, causal, dtype, &empty,
+                              h_kv);
+  if (st != ATTN_OK) return st;
+  if (num_splits < 0 || num_splits > 64) return ATTN_ERR_INVALID_ARG;
+  if (T_q < 2) return ATTN_ERR_INVALID_ARG;  // one query row: use the decode entries
+  if (empty) {
+    t_last_kernel = "none";
+    return ATTN_OK;
+  }
+  attn::FwdProblem p{q, k, v, o, lse, B, h_q, T_q, T_kv, d, scale, causal,
+                     dtype == ATTN_BF16 ? 1 : 0, nullptr, h_kv};
+  const int splits = num_splits > 0 ? num_splits : prefill_auto_splits(B, h_q, T_q, T_kv);
+  const bool own = workspace == nullptr && workspace_bytes == 0;
+  return run_prefill(p, splits, workspace, workspace_bytes, own, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_splitkv_workspace_bytes(int B, int h_q, int T_q, int T_kv, int d, int num_splits) {
+  if (B < 1 || h_q < 1 || T_q < 2 || T_kv < 1 || (d != 64 && d != 128)) return 0;
+  if (num_splits < 0 || num_splits > 64) return 0;
+  const int splits = num_splits > 0 ? num_splits : prefill_auto_splits(B, h_q, T_q, T_kv);
+  return prefill_ws_bytes(B, h_q, T_q, d, splits);
 }
 
 size_t attn_gqa_workspace_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int d,

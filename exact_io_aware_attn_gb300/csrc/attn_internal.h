@@ -23,9 +23,17 @@ struct FwdProblem {
   int h_kv;               // key/value heads; h is a multiple of it (h_kv == h: plain attention)
 };
 
-// Prefill (T_q > 1): tcgen05 tensor-core kernel. `name` receives a static
-// kernel name on success.
-cudaError_t launch_prefill(const FwdProblem& p, cudaStream_t stream, const char** name);
+// Prefill (T_q > 1): tcgen05 tensor-core kernel. With num_splits > 1 the
+// key range of every query-tile pair is cut into that many partitions whose
+// fp32 partials ([B*h*T_q][num_splits][d+4] at `part`) the merge kernel then
+// combines into o and lse. `name` receives a static kernel name on success.
+cudaError_t launch_prefill(const FwdProblem& p, int num_splits, float* part, cudaStream_t stream,
+                           const char** name);
+
+// The exact merge of per-row partials ([rows][S][d+4] fp32: o, m, l in log2
+// units) into 16-bit o [rows][d] and lse [rows] (decode_sm103.cu).
+cudaError_t launch_combine(const float* part, void* o, float* lse, long long rows, int S, int d,
+                           bool bf16, cudaStream_t stream);
 
 // Decode (T_q == 1): split kernel over `num_splits` key partitions writing
 // partials to `ws`, then the merge kernel.

@@ -731,6 +731,27 @@ cudaError_t launch_decode_paged(const PagedProblem& p, int num_splits, float* ws
   return e;
 }
 
+cudaError_t launch_combine(const float* part, void* o, float* lse, long long rows, int S, int d,
+                           bool bf16, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int n = static_cast<int>(rows);
+  uint8_t* out = static_cast<uint8_t*>(o);
+  if (d == 64)
+    return bf16 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<64, true>, part, out, lse, n, S)
+                : cudaLaunchKernelEx(&cfg, decode_combine_kernel<64, false>, part, out, lse, n, S);
+  return bf16 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<128, true>, part, out, lse, n, S)
+              : cudaLaunchKernelEx(&cfg, decode_combine_kernel<128, false>, part, out, lse, n, S);
+}
+
 int decode_paged_ctas_per_sm(int d) {
   int n = 0;
   const cudaError_t e =

@@ -190,14 +190,18 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 }
 
 // One work unit: query tiles A = rows [q0, q0+128) and B = [q0+128, q0+256)
-// of head bh, and how many key tiles each must see.
+// of head bh, key partition s of S: key tiles [j0, j0 + n_all), of which tile
+// A sees the first n_a and tile B the first n_b (causal: up to the diagonal).
+// With S = 1 the partition is every key tile the pair sees.
 struct Unit {
-  int bh, kvbh, q0, rows_b, n_a, n_b, n_all;
+  int bh, kvbh, q0, rows_b, n_a, n_b, n_all, j0, s;
 };
 
 __device__ __forceinline__ Unit unit_info(int u, int BH, int n_pairs, int T_q, int T_kv,
-                                          int causal, int h_q, int h_kv) {
+                                          int causal, int h_q, int h_kv, int S) {
   Unit w;
+  w.s = u % S;
+  u /= S;
   const int pair = n_pairs - 1 - u / BH;  // heaviest pairs first under a causal mask
   w.bh = u % BH;
   // grouped-query attention: query head i reads key/value head i / (h_q / h_kv)
@@ -215,6 +219,13 @@ __device__ __forceinline__ Unit unit_info(int u, int BH, int n_pairs, int T_q, i
   } else {
     w.n_b = 0;
   }
+  // key partition s of S: ceil(N/S) key tiles each, N = the pair's key tiles
+  const int n_full = max(w.n_a, w.n_b);
+  const int chunk = (n_full + S - 1) / S;
+  w.j0 = w.s * chunk;
+  const int span = max(0, min(n_full, w.j0 + chunk) - w.j0);
+  w.n_a = max(0, min(w.n_a - w.j0, span));
+  w.n_b = max(0, min(w.n_b - w.j0, span));
   w.n_all = max(w.n_a, w.n_b);
   return w;
 }
@@ -232,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmV, void* __restrict__ out,
                    float* __restrict__ lse, int T_q, int T_kv, int BH, int n_pairs,
                    float scale_log2, int causal, unsigned int* __restrict__ status, int h_q,
-                   int h_kv) {
+                   int h_kv, int S, float* __restrict__ part) {
   using C = Cfg<D>;
   constexpr int SL = C::SLOTS;
   extern __shared__ uint8_t smem_raw[];
@@ -254,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int U = n_pairs * BH;
+  // units: (query-tile pair, head, key partition); S > 1 writes fp32
+  // partials (o, m, l) to `part` for the merge kernel instead of O and lse
+  const int U = n_pairs * BH * S;
   const int G = static_cast<int>(gridDim.x);
   const int bid = static_cast<int>(blockIdx.x);
   const int off = T_kv - T_q;
@@ -307,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
+          if (w.n_all == 0) continue;  // a key partition the pair does not reach
           ok = ptx::mbar_wait(q_empty, (nq & 1) ^ 1, status, status_word(kKernPrefill, kSiteProdQ));
           if (!ok) break;
           ptx::mbar_arrive_expect_tx(q_full, C::TILE_BYTES * (w.rows_b > 0 ? 2 : 1));
@@ -331,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
                 ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot], c * 64,
-                                 j * kBN, w.kvbh, pol_kv);
+                                 (w.j0 + j) * kBN, w.kvbh, pol_kv);
               ++g;
             }
           }
@@ -441,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
+          if (w.n_all == 0) continue;  // skipped by the producer too
           ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
           ++nq;
           if (!ok) break;
@@ -490,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
+          if (w.n_all == 0) continue;  // skipped by the producer too
           ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
           ++nq;
           if (!ok) break;
@@ -557,10 +573,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; ok && rr * G < U; ++rr) {
       const int u = unit_of_round(rr, bid, G);
       if (u >= U) continue;
-      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv);
+      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
       const int n_x = x ? w.n_b : w.n_a;
-      if (n_x == 0) continue;
       const int row = w.q0 + x * kBM + r;        // absolute query row
+      if (n_x == 0) {
+        // no key of this partition for this tile: an empty partial (weight 0
+        // in the merge) for each of its rows
+        if (S > 1 && row < T_q && (x == 0 || w.rows_b > 0)) {
+          float* pr = part + ((static_cast<size_t>(w.bh) * T_q + row) * S + w.s) * (D + 4);
+#pragma unroll
+          for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(pr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(pr + D) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
       const int last_key = causal ? min(T_kv - 1, row + off) : T_kv - 1;
       float m_used = -INFINITY;  // reference max, log2 units of the scaled score
       float l = 0.f;
@@ -582,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float* s = reinterpret_cast<float*>(sr);
 
-        const int key0 = j * kBN;
+        const int key0 = (w.j0 + j) * kBN;
         if (key0 + kBN - 1 > last_key) {
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
@@ -672,8 +698,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const float inv_l = 1.f / l;
       const bool write = row < T_q;
+      if (S > 1) {
+        // partial of key partition s: unnormalised o, and (m, l) in log2
+        // units of the scaled score -- the decode partial format
+        float* pr = part + ((static_cast<size_t>(w.bh) * T_q + (write ? row : 0)) * S + w.s) * (D + 4);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t raw[32];
+          ptx::tmem_ld_32x32b_x32(t_o + c * 32, raw);
+          tmem_wait_ld_regs(raw);
+          if (write) {
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4)
+              *reinterpret_cast<float4*>(pr + c * 32 + g4 * 4) =
+                  make_float4(__uint_as_float(raw[4 * g4]), __uint_as_float(raw[4 * g4 + 1]),
+                              __uint_as_float(raw[4 * g4 + 2]), __uint_as_float(raw[4 * g4 + 3]));
+          }
+        }
+        if (write) *reinterpret_cast<float4*>(pr + D) = make_float4(m_used, l, 0.f, 0.f);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&o_empty[x]);
+        continue;
+      }
+      const float inv_l = 1.f / l;
       uint8_t* orow = reinterpret_cast<uint8_t*>(out) +
                       (static_cast<size_t>(w.bh) * T_q + (write ? row : 0)) * D * 2;
 #pragma unroll
@@ -713,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
 template <int D, bool BF16>
-cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
+cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = prefill_kernel<D, BF16>;
   static std::mutex mu;
@@ -738,27 +786,39 @@ cudaError_t launch_t(const FwdProblem& p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const int n_qtiles = (p.T_q + kBM - 1) / kBM;
   const int n_pairs = (n_qtiles + 1) / 2;
-  const long long units = static_cast<long long>(n_pairs) * BH;
+  const long long units = static_cast<long long>(n_pairs) * BH * S;
   const int sms = device_sms(dev);
   const int grid = static_cast<int>(units < sms ? units : sms);
   const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p.o, p.lse, p.T_q, p.T_kv, BH, n_pairs,
-                                                  scale_log2, p.causal, p.status, p.h, p.h_kv);
+                                                  scale_log2, p.causal, p.status, p.h, p.h_kv, S,
+                                                  part);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const FwdProblem& p, cudaStream_t stream, const char** name) {
+cudaError_t launch_prefill(const FwdProblem& p, int num_splits, float* part, cudaStream_t stream,
+                           const char** name) {
   cudaError_t e;
+  const bool split = num_splits > 1;
   if (p.d == 64) {
-    e = p.bf16 ? launch_t<64, true>(p, stream) : launch_t<64, false>(p, stream);
-    *name = p.bf16 ? "prefill_tcgen05_d64_bf16" : "prefill_tcgen05_d64_f16";
+    e = p.bf16 ? launch_t<64, true>(p, num_splits, part, stream)
+               : launch_t<64, false>(p, num_splits, part, stream);
+    *name = split ? (p.bf16 ? "prefill_splitkv_tcgen05_d64_bf16+decode_combine"
+                            : "prefill_splitkv_tcgen05_d64_f16+decode_combine")
+                  : (p.bf16 ? "prefill_tcgen05_d64_bf16" : "prefill_tcgen05_d64_f16");
   } else {
-    e = p.bf16 ? launch_t<128, true>(p, stream) : launch_t<128, false>(p, stream);
-    *name = p.bf16 ? "prefill_tcgen05_d128_bf16" : "prefill_tcgen05_d128_f16";
+    e = p.bf16 ? launch_t<128, true>(p, num_splits, part, stream)
+               : launch_t<128, false>(p, num_splits, part, stream);
+    *name = split ? (p.bf16 ? "prefill_splitkv_tcgen05_d128_bf16+decode_combine"
+                            : "prefill_splitkv_tcgen05_d128_f16+decode_combine")
+                  : (p.bf16 ? "prefill_tcgen05_d128_bf16" : "prefill_tcgen05_d128_f16");
   }
-  return e;
+  if (e != cudaSuccess || !split) return e;
+  // merge the partials of each query row: rows = B*h*T_q
+  return launch_combine(part, p.o, p.lse, static_cast<long long>(p.B) * p.h * p.T_q, num_splits,
+                        p.d, p.bf16 != 0, stream);
 }
 
 }  // namespace attn

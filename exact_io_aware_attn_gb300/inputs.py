@@ -79,7 +79,12 @@ WORKLOADS = [TINY, GPT2_PREFILL, LONG_4K, LONG_8K, LONG_8K_D128, VERY_LONG, DECO
 # heads share 8 key/value heads, the geometry of common grouped-query models.
 DECODE_GQA = Workload("decode_gqa_B32_hq32_hkv8_Tkv16384_d128_bf16", 32, 32, 1, 16384, 128, BF16,
                       False, h_kv=8)
-EXTRA_WORKLOADS = [DECODE_GQA]
+# Chunked prefill (also beyond the five): 256 new query rows of one sequence
+# against a 16K-token causal context, the shape where one CTA per query-tile
+# pair leaves most SMs idle and the key range is split.
+CHUNKED_PREFILL = Workload("chunked_prefill_B1_h8_Tq256_Tkv16384_d128_bf16", 1, 8, 256, 16384, 128,
+                           BF16, True)
+EXTRA_WORKLOADS = [DECODE_GQA, CHUNKED_PREFILL]
 
 
 def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu", h_kv=None):

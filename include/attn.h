@@ -28,7 +28,9 @@
  * Dispatch: T_q == 1 runs the split-KV decode path (a split kernel over key
  * partitions, then an exact merge kernel: "IO-Aware Attention ...", section
  * "Parallelism and the cost of the split"); T_q > 1 runs the tensor-core
- * prefill kernel.
+ * prefill kernel -- attn_fwd also cuts its key range into partitions when
+ * B*h*ceil(T_q/256) units would fill less than half the SMs (see
+ * attn_fwd_splitkv).
  *
  * Conventions for every entry point:
  *   - Tensors are dense, row-major, contiguous [B][h][T][d] in device memory,
@@ -287,6 +289,35 @@ attn_status_t attn_fwd_paged_decode(const void* q, const void* k_pages, const vo
  */
 size_t attn_paged_workspace_bytes(int B, int h_q, int d, int page_size, int max_pages_per_seq,
                                   int num_splits);
+
+/*
+ * attn_fwd_splitkv -- the prefill path (T_q > 1) with the key range of every
+ * pair of 128-row query tiles cut into num_splits partitions: for short
+ * queries against a long context, or a small batch x heads, where one CTA
+ * per query-tile pair would leave most SMs idle. Each partition writes an
+ * fp32 partial (unnormalised o, running max, running sum) per query row and
+ * an exact merge combines them ("IO-Aware Attention: Tiling the Score Matrix
+ * Without Materializing It", section "Parallelism and the cost of the
+ * split": partitions over keys, merged with the same rescaling).
+ *
+ * Arguments as attn_fwd_gqa (h_kv == h_q for plain attention); T_q >= 2
+ * (ATTN_ERR_INVALID_ARG otherwise: one row is the decode path).
+ * num_splits: 0 = the library's choice (1 when the units already fill half
+ * the SMs), else 1..64 (1 = the plain prefill kernel). workspace: at least
+ * attn_splitkv_workspace_bytes(...) bytes (B*h_q*T_q*S*(d+4)*4; 0 when
+ * S = 1), 16-byte aligned, not overlapping any argument, or NULL with
+ * workspace_bytes 0 to have the library take it stream-ordered. attn_fwd
+ * makes the same choice by itself; attn_fwd_ex and attn_fwd_gqa with a
+ * caller workspace never split the prefill.
+ */
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int h_q, int h_kv, int T_q, int T_kv, int d, float scale,
+                               int causal, int dtype, int num_splits, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* attn_splitkv_workspace_bytes -- workspace attn_fwd_splitkv needs (0 for
+ * invalid sizes or one partition). */
+size_t attn_splitkv_workspace_bytes(int B, int h_q, int T_q, int T_kv, int d, int num_splits);
 
 /*
  * attn_fwd_decode_noalloc -- the decode path (T_q == 1) without any

@@ -323,3 +323,34 @@ def test_paged_workspace_bytes(L):
     assert _lib.paged_workspace_bytes(2, 4, 128, 16, 8, 3) == 2 * 4 * 3 * 132 * 4
     assert _lib.paged_workspace_bytes(2, 4, 64, 24, 8, 5) == 0
     assert _lib.paged_workspace_bytes(0, 4, 64, 16, 8, 5) == 0
+
+
+def _splitkv(**over):
+    a = dict(B=1, h_q=4, h_kv=2, T_q=256, T_kv=4096, d=64, scale=0.125, causal=1,
+             dtype=_lib.ATTN_BF16, num_splits=8)
+    ws, nbytes = over.pop("ws", None), over.pop("nbytes", 0)
+    a.update(over)
+    return _lib.splitkv_raw(Q, K, V, O, LSE, a["B"], a["h_q"], a["h_kv"], a["T_q"], a["T_kv"],
+                            a["d"], a["scale"], a["causal"], a["dtype"], a["num_splits"], ws,
+                            nbytes, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(T_q=1), _lib.ATTN_ERR_INVALID_ARG),            # one row: the decode path
+    (dict(num_splits=65), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(num_splits=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(h_kv=3), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(T_q=5000, T_kv=4096), _lib.ATTN_ERR_INVALID_ARG),   # causal needs T_q <= T_kv
+    (dict(ws=WS, nbytes=64), _lib.ATTN_ERR_WORKSPACE),   # too small for 8 partitions
+    (dict(ws=Q, nbytes=1 << 30), _lib.ATTN_ERR_WORKSPACE),  # overlaps q
+    (dict(B=0), _lib.ATTN_OK),
+])
+def test_splitkv_arguments(L, over, status):
+    assert _splitkv(**over) == status
+
+
+def test_splitkv_workspace_bytes(L):
+    assert _lib.splitkv_workspace_bytes(1, 4, 256, 4096, 64, 8) == 4 * 256 * 8 * 68 * 4
+    assert _lib.splitkv_workspace_bytes(1, 4, 256, 4096, 64, 1) == 0
+    assert _lib.splitkv_workspace_bytes(1, 4, 1, 4096, 64, 8) == 0
