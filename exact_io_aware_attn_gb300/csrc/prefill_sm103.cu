@@ -274,10 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    ptx::mbar_init(q_empty, 1);
+    // released by each MMA-issuing warp (two at d = 64: one per tile)
+    ptx::mbar_init(q_empty, C::SEP_P ? 2 : 1);
     for (int i = 0; i < SL; ++i) {
       ptx::mbar_init(&slot_full[i], 1);
-      ptx::mbar_init(&slot_empty[i], 1);
+      ptx::mbar_init(&slot_empty[i], C::SEP_P ? 2 : 1);
     }
     for (int x = 0; x < 2; ++x) {
       ptx::mbar_init(&s_full[x], 1);
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&o_full[x], 1);
       ptx::mbar_init(&o_empty[x], 128);
     }
-    ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(mma_done, C::SEP_P ? 2 : 1);
     for (int x = 0; x < 2; ++x) {
       ptx::mbar_init(&s_free[x], 128);
       ptx::mbar_init(&pv_done[x], 1);
@@ -359,8 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(&slot_full[i % SL], (i / SL) & 1);
         }
       }
-    } else if (warp == kWarpMma) {
-      // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kWarpMma || (C::SEP_P && warp == kWarpMma + 1)) {
+      // ------------------------------------------------------------ MMA issuer(s)
+      // d = 64: warp 9 issues tile A's products and warp 10 tile B's, each in
+      // the order its own barriers allow; shared K/V slots and the Q buffer
+      // are released by a commit from each. d = 128: warp 9 issues both.
+      const int xi = warp - kWarpMma;
       // The whole warp runs this loop in uniform control flow, so descriptor
       // arithmetic stays warp-uniform; one elected lane (the lowest active
       // one, the same every time) issues each batch of MMAs and every commit,
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
       const uint32_t sRing = ptx::smem_u32(smem + C::OFF_RING);
       uint32_t g = 0, nq = 0;
-      uint32_t np[2] = {0, 0}, noe[2] = {0, 0};
+      uint32_t np0 = 0, np1 = 0, noe0 = 0, noe1 = 0;
       bool ok = true;
 
       auto wait_bar = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
@@ -415,13 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       auto wait_p = [&](int x, bool first) {
-        bool good = wait_bar(&p_full[x], np[x] & 1, kSiteMmaP);
-        ++np[x];
+        // (scalar counters per tile: an array indexed by the tile would live
+        // in local memory)
+        bool good = wait_bar(&p_full[x], (x ? np1 : np0) & 1, kSiteMmaP);
+        if (x) ++np1; else ++np0;
         if (good && first) {
           // O_X is overwritten by this unit's first product: the previous
           // unit's epilogue must have read it.
-          good = wait_bar(&o_empty[x], (noe[x] & 1) ^ 1, kSiteMmaOEmpty);
-          ++noe[x];
+          good = wait_bar(&o_empty[x], ((x ? noe1 : noe0) & 1) ^ 1, kSiteMmaOEmpty);
+          if (x) ++noe1; else ++noe0;
         }
         ptx::tc_fence_after();
         return good;
@@ -429,13 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if constexpr (C::SEP_P) {
         // S_X(t) may overwrite S_X once the softmax has read S_X(t-1)
-        uint32_t ns_iss[2] = {0, 0};
+        uint32_t ns_iss = 0;  // score products this warp issued (its tile only)
         auto issue_s_sep = [&](int x, uint32_t kslot) {
-          if (ns_iss[x] > 0 && !wait_bar(&s_free[x], (ns_iss[x] - 1) & 1, kSiteMmaSFree))
-            return false;
+          if (ns_iss > 0 && !wait_bar(&s_free[x], (ns_iss - 1) & 1, kSiteMmaSFree)) return false;
           ptx::tc_fence_after();
           issue_s(x, kslot);
-          ++ns_iss[x];
+          ++ns_iss;
           return true;
         };
         auto issue_pv_sep = [&](int x, uint32_t vslot, bool first) {
@@ -452,22 +458,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         };
+        const int x = xi;  // this warp's tile
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
           const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
           if (w.n_all == 0) continue;  // skipped by the producer too
+          const int n_x = x ? w.n_b : w.n_a;
           ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
           ++nq;
           if (!ok) break;
           ok = wait_slot(g);  // K_0
           if (!ok) break;
           ptx::tc_fence_after();
-          ok = issue_s_sep(0, g % SL);
-          if (ok && w.n_b > 0) ok = issue_s_sep(1, g % SL);
+          if (n_x > 0) ok = issue_s_sep(x, g % SL);
           if (!ok) break;
           commit(&slot_empty[g % SL]);
-          if (w.n_all == 1) commit(q_empty);
+          if (n_x <= 1) commit(q_empty);  // no further score product of this tile reads Q
           for (int j = 0; j < w.n_all; ++j) {
             const uint32_t vi = g + 2 * j + 1;  // V_j
             const uint32_t ki = vi + 1;         // K_{j+1}
@@ -477,25 +484,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = wait_slot(ki);
               if (!ok) break;
               ptx::tc_fence_after();
-              if (j + 1 < w.n_a) ok = issue_s_sep(0, ki % SL);
-              if (ok && j + 1 < w.n_b) ok = issue_s_sep(1, ki % SL);
+              if (j + 1 < n_x) ok = issue_s_sep(x, ki % SL);
               if (!ok) break;
               commit(&slot_empty[ki % SL]);
-              if (j + 2 == w.n_all) commit(q_empty);
+              if (j + 2 == n_x) commit(q_empty);
             }
             ok = wait_slot(vi);
             if (!ok) break;
-            if (j < w.n_a) {
-              ok = wait_p(0, j == 0);
+            if (j < n_x) {
+              ok = wait_p(x, j == 0);
               if (!ok) break;
-              issue_pv_sep(0, vi % SL, j == 0);
-              if (j == w.n_a - 1) commit(&o_full[0]);
-            }
-            if (j < w.n_b) {
-              ok = wait_p(1, j == 0);
-              if (!ok) break;
-              issue_pv_sep(1, vi % SL, j == 0);
-              if (j == w.n_b - 1) commit(&o_full[1]);
+              issue_pv_sep(x, vi % SL, j == 0);
+              if (j == n_x - 1) commit(&o_full[x]);
             }
             commit(&slot_empty[vi % SL]);
           }
