@@ -184,7 +184,19 @@ long long decode_rows(int B, int h, int h_kv) {
   return static_cast<long long>(B) * h_kv * (g / attn::decode_heads_per_cta(g));
 }
 
+// Grouped-query decode with at least this many query heads per key/value
+// head runs on the tensor cores: the group's query rows are contiguous in q
+// ([B][h_q][1][d] is [B][h_kv][G][d]), so the decode is a non-causal prefill
+// of T_q = G rows per key/value head, cut into key partitions and merged
+// exactly (the split-KV prefill). The CUDA-core split kernel does
+// 2*d*G FMAs per cached key and runs out of issue slots at large G.
+constexpr int kTensorGroup = 4;
+bool gqa_decode_on_tensor_cores(int h, int h_kv) { return h_kv > 0 && h / h_kv >= kTensorGroup; }
+
 int auto_splits(int B, int h, int h_kv, int T_kv, int d) {
+  if (gqa_decode_on_tensor_cores(h, h_kv))  // one prefill CTA per SM
+    return std::min(64, attn::detail::choose_splits_cap(static_cast<long long>(B) * h_kv, T_kv,
+                                                        sm_count()));
   return choose_splits(decode_rows(B, h, h_kv), T_kv, d, attn::decode_heads_per_cta(h / h_kv));
 }
 
@@ -271,6 +283,15 @@ attn_status_t run(const void* q, const void* k, const void* v, void* o, float* l
   // the same choice attn_workspace_bytes(..., 0) reports (occupancy of the bf16
   // and fp16 split kernels is identical)
   const int splits = num_splits > 0 ? num_splits : auto_splits(B, h, h_kv, T_kv, d);
+  if (gqa_decode_on_tensor_cores(h, h_kv)) {
+    // the G = h/h_kv query heads of each key/value head as G query rows
+    // of one virtual head: B*h_kv heads, T_q = G, no mask; partials and
+    // outputs land in the same [B*h][...] order as the decode's
+    if (splits > 64) return ATTN_ERR_UNSUPPORTED;
+    attn::FwdProblem g{q, k, v, o, lse, B, h_kv, h / h_kv, T_kv, d, scale, 0,
+                       dtype == ATTN_BF16 ? 1 : 0, nullptr, h_kv};
+    return run_prefill(g, splits, workspace, workspace_bytes, own_workspace, s);
+  }
   // split grid: one CTA per (row of query heads, partition)
   if (decode_rows(B, h, h_kv) * splits > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
   const size_t need = ws_bytes(B, h, d, splits);

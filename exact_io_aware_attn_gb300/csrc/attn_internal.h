@@ -92,11 +92,10 @@ cudaError_t launch_decode_paged(const PagedProblem& p, int num_splits, float* ws
                                 cudaStream_t stream, const char** name);
 int decode_paged_ctas_per_sm(int d);
 
-// Query heads one decode split CTA serves (all sharing one key/value head):
-// the largest of 8, 4, 2, 1 that divides the group size h / h_kv.
-inline int decode_heads_per_cta(int group) {
-  return (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : (group % 2 == 0) ? 2 : 1;
-}
+// Query heads one CUDA-core decode split CTA serves (all sharing one
+// key/value head): 2 for even groups, else 1. Groups of 4 or more query heads
+// per key/value head decode on the tensor cores instead (attn_api.cu).
+inline int decode_heads_per_cta(int group) { return (group % 2 == 0) ? 2 : 1; }
 
 // Split kernel occupancy (CTAs per SM) for the split-count heuristic.
 int decode_split_ctas_per_sm(int d, int heads_per_cta);

@@ -361,8 +361,12 @@ __global__ void __launch_bounds__(kDecThreads)
 }
 
 // One CTA: partition s of the keys of one key/value head, for G query heads
-// that share it (grouped-query attention; G = 1 for plain attention). Every
-// cached key and value row is read once and used for all G heads.
+// that share it (grouped-query attention with an even group below 4; groups
+// of 4 or more decode on the tensor cores). Every cached key and value row is
+// read once and used for all G heads. Measured on GB300: at G = 4 and 8 the
+// 2*d*G FMAs and G dot-product shuffle trees per cached key leave the kernel
+// issue-bound (59% and 17% of HBM at d = 128), which is why larger groups
+// take the tensor-core path.
 template <int D, bool BF16, int G>
 __global__ void __launch_bounds__(kDecThreads)
     decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kDecThreads)
   constexpr int KPW = 32 / TPK;         // keys per warp per load
   constexpr int SLOTS = (kDecThreads / 32) * KPW;
   constexpr int ROW = D * 2;            // bytes per key row
-  constexpr int UNR = (G >= 8) ? 1 : (G >= 4) ? 2 : kUnroll;  // keys in flight per thread
+  constexpr int UNR = (G >= 4) ? 2 : kUnroll;  // keys in flight per thread (registers)
 
   const int s = static_cast<int>(blockIdx.x % static_cast<unsigned>(S));
   const int grp = static_cast<int>(blockIdx.x / static_cast<unsigned>(S));
@@ -631,8 +635,6 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* ws, cudaStream_t stream)
 template <int D, bool BF16>
 cudaError_t launch_g(const FwdProblem& p, int S, float* ws, cudaStream_t stream) {
   switch (decode_heads_per_cta(p.h / p.h_kv)) {
-    case 8: return launch_t<D, BF16, 8>(p, S, ws, stream);
-    case 4: return launch_t<D, BF16, 4>(p, S, ws, stream);
     case 2: return launch_t<D, BF16, 2>(p, S, ws, stream);
     default: return launch_t<D, BF16, 1>(p, S, ws, stream);
   }
@@ -694,15 +696,11 @@ int decode_split_ctas_per_sm(int d, int heads_per_cta) {
   auto occ = [&](auto kern) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecThreads, smem); };
   if (d == 64) {
     switch (heads_per_cta) {
-      case 8: e = occ(decode_split_kernel<64, true, 8>); break;
-      case 4: e = occ(decode_split_kernel<64, true, 4>); break;
       case 2: e = occ(decode_split_kernel<64, true, 2>); break;
       default: e = occ(decode_split_1head_kernel<64, true>); break;
     }
   } else {
     switch (heads_per_cta) {
-      case 8: e = occ(decode_split_kernel<128, true, 8>); break;
-      case 4: e = occ(decode_split_kernel<128, true, 4>); break;
       case 2: e = occ(decode_split_kernel<128, true, 2>); break;
       default: e = occ(decode_split_1head_kernel<128, true>); break;
     }
