@@ -150,3 +150,30 @@ def test_backward_kernel_name():
     _lib.attn_bwd(q, k, v, o, lse, torch.ones_like(q))
     torch.cuda.synchronize()
     assert _lib.last_kernel_name() == "bwd_prep+bwd_dkdv+bwd_dq_tcgen05_d128_f16"
+
+
+@pytest.mark.parametrize("case", [
+    # B, h, T, d, dtype, heads checked
+    (1, 16, 4096, 128, BF16, ((0, 0), (0, 13))),
+    (1, 8, 4096, 64, F16, ((0, 3),)),
+])
+def test_backward_long_sampled_heads(case):
+    """Long causal backward in one call; whole heads checked against the
+    oracle run on those heads alone (the oracle materialises T x T per head)."""
+    B, h, T, d, dt, heads = case
+    q, k, v = make_qkv(B, h, T, T, d, dt, seed=38)
+    do = make_dout(B, h, T, d, dt, seed=38)
+    got = gpu_bwd(q, k, v, do, True)
+    for (b, hh) in heads:
+        sl = (slice(b, b + 1), slice(hh, hh + 1))
+        ref = oracle_bwd(q[sl], k[sl], v[sl], do[sl], True)
+        compare_grads(tuple(g[sl] for g in got), ref, dt, f"long bwd {case[:5]} head {(b, hh)}")
+
+
+def test_backward_gqa_moderate_size():
+    """Grouped-query backward, 8 query heads on 2 key/value heads, T 1024:
+    each dK/dV CTA sums four query heads' contributions."""
+    q, k, v = make_qkv(2, 8, 1024, 1024, 64, BF16, seed=39, h_kv=2)
+    do = make_dout(2, 8, 1024, 64, BF16, seed=39)
+    got = gpu_bwd(q, k, v, do, True)
+    compare_grads(got, oracle_bwd(q, k, v, do, True), BF16, "gqa bwd T1024")
