@@ -48,7 +48,7 @@ SIGNATURES = {
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_fwd_paged_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
                                    _F, _I, _I, _VP, _SZ, _VP]),
-    "attn_paged_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_paged_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "attn_fwd_splitkv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP,
                               _SZ, _VP]),
     "attn_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -344,8 +344,8 @@ def attn_bwd(q, k, v, o, lse, dout, *, scale=None, causal=False, dq=None, dk=Non
     return dq, dk, dv
 
 
-def paged_workspace_bytes(B, h_q, d, page_size, max_pages_per_seq, num_splits=0) -> int:
-    return int(lib().attn_paged_workspace_bytes(B, h_q, d, page_size, max_pages_per_seq,
+def paged_workspace_bytes(B, h_q, h_kv, d, page_size, max_pages_per_seq, num_splits=0) -> int:
+    return int(lib().attn_paged_workspace_bytes(B, h_q, h_kv, d, page_size, max_pages_per_seq,
                                                 num_splits))
 
 

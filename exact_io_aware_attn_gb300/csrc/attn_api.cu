@@ -192,6 +192,12 @@ long long decode_rows(int B, int h, int h_kv) {
 // 2*d*G FMAs per cached key and runs out of issue slots at large G.
 constexpr int kTensorGroup = 4;
 bool gqa_decode_on_tensor_cores(int h, int h_kv) { return h_kv > 0 && h / h_kv >= kTensorGroup; }
+// Paged decode with groups of kTensorGroup or more and pages of at least 8
+// rows (whole 1024-byte swizzle atoms per TMA box) runs on the tensor cores:
+// the prefill kernel gathering K/V tiles through the block table.
+bool paged_on_tensor_cores(int h_q, int h_kv, int page_size) {
+  return gqa_decode_on_tensor_cores(h_q, h_kv) && page_size >= 8;
+}
 
 int auto_splits(int B, int h, int h_kv, int T_kv, int d) {
   if (gqa_decode_on_tensor_cores(h, h_kv))  // one prefill CTA per SM
@@ -394,9 +400,12 @@ int paged_ctas_per_sm(int d) {
 
 // Paged decode: the split count for a shape, from the longest cache the
 // block table can name (the lengths live on the device).
-int paged_auto_splits(int B, int h_q, int d, int page_size, int max_pages) {
-  const long long cap = static_cast<long long>(sm_count()) * paged_ctas_per_sm(d);
+int paged_auto_splits(int B, int h_q, int h_kv, int d, int page_size, int max_pages) {
   const long long t = std::min<long long>(0x7fffffffll, static_cast<long long>(page_size) * max_pages);
+  if (paged_on_tensor_cores(h_q, h_kv, page_size))  // one prefill CTA per SM
+    return std::min(64, attn::detail::choose_splits_cap(static_cast<long long>(B) * h_kv,
+                                                        static_cast<int>(t), sm_count()));
+  const long long cap = static_cast<long long>(sm_count()) * paged_ctas_per_sm(d);
   return attn::detail::choose_splits_cap(static_cast<long long>(B) * h_q, static_cast<int>(t), cap);
 }
 
@@ -426,7 +435,8 @@ attn_status_t run_paged(const void* q, const void* k_pages, const void* v_pages,
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(o, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
     return ATTN_ERR_INVALID_ARG;
-  const int splits = num_splits > 0 ? num_splits : paged_auto_splits(B, h_q, d, page_size, max_pages);
+  const int splits =
+      num_splits > 0 ? num_splits : paged_auto_splits(B, h_q, h_kv, d, page_size, max_pages);
   if (BH * splits > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
   const size_t qo = static_cast<size_t>(BH) * d * 2;
   const size_t pool = static_cast<size_t>(num_pages) * h_kv * page_size * d * 2;
@@ -438,9 +448,11 @@ attn_status_t run_paged(const void* q, const void* k_pages, const void* v_pages,
   for (const Buf& b : ins)
     if (overlaps(o, qo, b.p, b.n) || overlaps(lse, lse_b, b.p, b.n)) return ATTN_ERR_INVALID_ARG;
   if (overlaps(o, qo, lse, lse_b)) return ATTN_ERR_INVALID_ARG;
-  const size_t need = ws_bytes(B, h_q, d, splits);
+  // (the tensor-core path with one partition writes o directly: no workspace)
+  const bool tc = paged_on_tensor_cores(h_q, h_kv, page_size);
+  const size_t need = (tc && splits <= 1) ? 0 : ws_bytes(B, h_q, d, splits);
   const bool own = workspace == nullptr && workspace_bytes == 0;
-  if (!own) {
+  if (!own && need > 0) {
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ATTN_ERR_WORKSPACE;
     for (const Buf& b : ins)
       if (overlaps(workspace, need, b.p, b.n)) return ATTN_ERR_WORKSPACE;
@@ -449,6 +461,25 @@ attn_status_t run_paged(const void* q, const void* k_pages, const void* v_pages,
   }
   int shift = 0;
   while ((1 << shift) < page_size) ++shift;
+  if (tc) {
+    if (splits > 64) return ATTN_ERR_UNSUPPORTED;
+    // virtual problem: B*h_kv heads of T_q = G query rows against the pages
+    attn::FwdProblem g{q, k_pages, v_pages, o, lse, B, h_kv, h_q / h_kv, page_size * max_pages, d,
+                       scale, 0, dtype == ATTN_BF16 ? 1 : 0, status_ptr(), h_kv};
+    if (!g.status) return ATTN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* ws = static_cast<float*>(workspace);
+    if (own && splits > 1 &&
+        cudaMallocAsync(reinterpret_cast<void**>(&ws), need, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    const char* name = "none";
+    const cudaError_t e = attn::launch_prefill_paged(g, block_table, seq_lens, shift, max_pages,
+                                                     num_pages, splits, ws, s, &name);
+    if (own && splits > 1) cudaFreeAsync(ws, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_kernel = name;
+    return ATTN_OK;
+  }
   attn::PagedProblem p{q, k_pages, v_pages, block_table, seq_lens, o, lse, B, h_q, h_kv, d, shift,
                        max_pages, num_pages, scale, dtype == ATTN_BF16 ? 1 : 0, status_ptr()};
   if (!p.status) return ATTN_ERR_CUDA;
@@ -569,14 +600,17 @@ attn_status_t attn_fwd_paged_decode(const void* q, const void* k_pages, const vo
                    workspace_bytes, stream);
 }
 
-size_t attn_paged_workspace_bytes(int B, int h_q, int d, int page_size, int max_pages_per_seq,
-                                  int num_splits) {
-  if (B < 1 || h_q < 1 || (d != 64 && d != 128) || !pow2(page_size) || page_size > 65536 ||
-      max_pages_per_seq < 1 || num_splits < 0 || num_splits > kMaxSplits)
+size_t attn_paged_workspace_bytes(int B, int h_q, int h_kv, int d, int page_size,
+                                  int max_pages_per_seq, int num_splits) {
+  if (B < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || (d != 64 && d != 128) ||
+      !pow2(page_size) || page_size > 65536 || max_pages_per_seq < 1 || num_splits < 0 ||
+      num_splits > kMaxSplits)
     return 0;
   if (static_cast<long long>(page_size) * max_pages_per_seq > 0x7fffffffll) return 0;
-  const int splits =
-      num_splits > 0 ? num_splits : paged_auto_splits(B, h_q, d, page_size, max_pages_per_seq);
+  const int splits = num_splits > 0 ? num_splits
+                                    : paged_auto_splits(B, h_q, h_kv, d, page_size,
+                                                        max_pages_per_seq);
+  if (paged_on_tensor_cores(h_q, h_kv, page_size) && splits <= 1) return 0;
   return ws_bytes(B, h_q, d, splits);
 }
 

@@ -30,6 +30,14 @@ struct FwdProblem {
 cudaError_t launch_prefill(const FwdProblem& p, int num_splits, float* part, cudaStream_t stream,
                            const char** name);
 
+// Grouped-query decode against a paged cache on the tensor cores: the prefill
+// kernel with K/V tiles gathered from the pool through the block table. p is
+// the virtual problem (B, h = h_kv, T_q = G query heads per key/value head,
+// T_kv = the longest length the table can name, no mask), p.k/p.v the pools.
+cudaError_t launch_prefill_paged(const FwdProblem& p, const int* table, const int* lens,
+                                 int page_shift, int max_pages, int num_pages, int num_splits,
+                                 float* part, cudaStream_t stream, const char** name);
+
 // The exact merge of per-row partials ([rows][S][d+4] fp32: o, m, l in log2
 // units) into 16-bit o [rows][d] and lse [rows] (decode_sm103.cu).
 cudaError_t launch_combine(const float* part, void* o, float* lse, long long rows, int S, int d,

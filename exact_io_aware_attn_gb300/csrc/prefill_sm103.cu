@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "attn_status.h"
 #include "ptx_sm103.cuh"
 #include "tma_host.h"
 
@@ -107,7 +108,7 @@ __host__ __device__ constexpr uint32_t col_p(int x) { return 384u + static_cast<
 // Wait sites recorded in the status word on a timeout.
 enum : uint32_t {
   kSiteProdQ = 1, kSiteProdSlot, kSiteMmaQ, kSiteMmaSlot, kSiteMmaP, kSiteMmaOEmpty,
-  kSiteSoftS, kSiteSoftO, kSiteMmaSFree, kSiteSoftPv
+  kSiteSoftS, kSiteSoftO, kSiteMmaSFree, kSiteSoftPv, kSiteBadPage
 };
 
 template <bool BF16>
@@ -194,16 +195,31 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 // A sees the first n_a and tile B the first n_b (causal: up to the diagonal).
 // With S = 1 the partition is every key tile the pair sees.
 struct Unit {
-  int bh, kvbh, q0, rows_b, n_a, n_b, n_all, j0, s;
+  int bh, kvbh, q0, rows_b, n_a, n_b, n_all, j0, s, tkv;
+};
+
+// Keys from a paged pool ([num_pages][h_kv][page_size][d]) through a block
+// table (int32 [B][max_pages]) with per-sequence lengths: the mode that runs
+// grouped-query decode against a paged cache (virtual head bh = b*h_kv + kv
+// head, its G query heads as query rows). table == nullptr: contiguous K/V.
+struct PagedKV {
+  const int* table;
+  const int* lens;
+  int page_shift, max_pages, num_pages;
 };
 
 __device__ __forceinline__ Unit unit_info(int u, int BH, int n_pairs, int T_q, int T_kv,
-                                          int causal, int h_q, int h_kv, int S) {
+                                          int causal, int h_q, int h_kv, int S,
+                                          const int* lens = nullptr) {
   Unit w;
   w.s = u % S;
   u /= S;
   const int pair = n_pairs - 1 - u / BH;  // heaviest pairs first under a causal mask
   w.bh = u % BH;
+  // paged mode: this sequence's length (b = bh / h_q), clamped to what its
+  // table can name (T_kv); otherwise every head has T_kv keys
+  w.tkv = lens ? max(0, min(__ldg(lens + w.bh / h_q), T_kv)) : T_kv;
+  T_kv = w.tkv;
   // grouped-query attention: query head i reads key/value head i / (h_q / h_kv)
   w.kvbh = (w.bh / h_q) * h_kv + (w.bh % h_q) / (h_q / h_kv);
   w.q0 = pair * 2 * kBM;
@@ -237,13 +253,13 @@ __device__ __forceinline__ int unit_of_round(int r, int bid, int G) {
   return (r & 1) ? r * G + (G - 1 - bid) : r * G + bid;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, void* __restrict__ out,
                    float* __restrict__ lse, int T_q, int T_kv, int BH, int n_pairs,
                    float scale_log2, int causal, unsigned int* __restrict__ status, int h_q,
-                   int h_kv, int S, float* __restrict__ part) {
+                   int h_kv, int S, float* __restrict__ part, const PagedKV pkv) {
   using C = Cfg<D>;
   constexpr int SL = C::SLOTS;
   extern __shared__ uint8_t smem_raw[];
@@ -321,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
           if (w.n_all == 0) continue;  // a key partition the pair does not reach
           ok = ptx::mbar_wait(q_empty, (nq & 1) ^ 1, status, status_word(kKernPrefill, kSiteProdQ));
           if (!ok) break;
@@ -343,10 +359,38 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
               ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
               uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+              if constexpr (PAGED) {
+                // the tile's 128 keys in boxes of min(page_size, 128) rows, each
+                // from the page the table names (rows past the length: page 0,
+                // masked later; a bad entry is reported, never dereferenced)
+                const int rows = min(1 << pkv.page_shift, kBN);
+                const int b = w.bh / h_q;  // sequence of this virtual head
+                const int kvh = w.bh - b * h_q;
+                for (int i = 0; i < kBN; i += rows) {
+                  const int key = (w.j0 + j) * kBN + i;
+                  int pg = 0;
+                  if (key < w.tkv) {
+                    pg = __ldg(pkv.table + static_cast<size_t>(b) * pkv.max_pages +
+                               (key >> pkv.page_shift));
+                    if (static_cast<unsigned>(pg) >= static_cast<unsigned>(pkv.num_pages)) {
+                      atomicCAS(status, 0u,
+                                status_word_code(1u /* ATTN_ERR_INVALID_ARG */, kKernPrefill,
+                                                 kSiteBadPage));
+                      pg = 0;
+                    }
+                  }
 #pragma unroll
-              for (int c = 0; c < D / 64; ++c)
-                ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot], c * 64,
-                                 (w.j0 + j) * kBN, w.kvbh, pol_kv);
+                  for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_load_3d(dst + c * kSub + i * 128, kind ? &tmV : &tmK,
+                                     &slot_full[slot], c * 64, key & ((1 << pkv.page_shift) - 1),
+                                     pg * h_q + kvh, pol_kv);
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                  ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot], c * 64,
+                                   (w.j0 + j) * kBN, w.kvbh, pol_kv);
+              }
               ++g;
             }
           }
@@ -462,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
           if (w.n_all == 0) continue;  // skipped by the producer too
           const int n_x = x ? w.n_b : w.n_a;
           ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
@@ -505,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
+          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
           if (w.n_all == 0) continue;  // skipped by the producer too
           ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
           ++nq;
@@ -573,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; ok && rr * G < U; ++rr) {
       const int u = unit_of_round(rr, bid, G);
       if (u >= U) continue;
-      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S);
+      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
       const int n_x = x ? w.n_b : w.n_a;
       const int row = w.q0 + x * kBM + r;        // absolute query row
       if (n_x == 0) {
@@ -587,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const int last_key = causal ? min(T_kv - 1, row + off) : T_kv - 1;
+      const int last_key = causal ? min(w.tkv - 1, row + off) : w.tkv - 1;
       float m_used = -INFINITY;  // reference max, log2 units of the scaled score
       float l = 0.f;
 
@@ -760,10 +804,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
-template <int D, bool BF16>
-cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t stream) {
+template <int D, bool BF16, bool PAGED>
+cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t stream,
+                     const PagedKV& pkv, const void* k_pool, const void* v_pool) {
   using C = Cfg<D>;
-  auto kern = prefill_kernel<D, BF16>;
+  auto kern = prefill_kernel<D, BF16, PAGED>;
   static std::mutex mu;
   static uint64_t configured = 0;  // one bit per device ordinal
   int dev = 0;
@@ -780,10 +825,18 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t strea
   const int BH = p.B * p.h;
   CUtensorMap mq, mk, mv;
   const int BH_kv = p.B * p.h_kv;
-  if (!make_map(&mq, p.q, p.T_q, BH, D, BF16, kBM) ||
-      !make_map(&mk, p.k, p.T_kv, BH_kv, D, BF16, kBN) ||
-      !make_map(&mv, p.v, p.T_kv, BH_kv, D, BF16, kBN))
-    return cudaErrorInvalidValue;
+  if (!make_map(&mq, p.q, p.T_q, BH, D, BF16, kBM)) return cudaErrorInvalidValue;
+  if constexpr (PAGED) {
+    // the pool as [num_pages * h_kv][page_size][D], boxes of min(page_size, 128) rows
+    const int ps = 1 << pkv.page_shift;
+    if (!make_map(&mk, k_pool, ps, pkv.num_pages * p.h_kv, D, BF16, ps < kBN ? ps : kBN) ||
+        !make_map(&mv, v_pool, ps, pkv.num_pages * p.h_kv, D, BF16, ps < kBN ? ps : kBN))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&mk, p.k, p.T_kv, BH_kv, D, BF16, kBN) ||
+        !make_map(&mv, p.v, p.T_kv, BH_kv, D, BF16, kBN))
+      return cudaErrorInvalidValue;
+  }
   const int n_qtiles = (p.T_q + kBM - 1) / kBM;
   const int n_pairs = (n_qtiles + 1) / 2;
   const long long units = static_cast<long long>(n_pairs) * BH * S;
@@ -792,7 +845,7 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t strea
   const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p.o, p.lse, p.T_q, p.T_kv, BH, n_pairs,
                                                   scale_log2, p.causal, p.status, p.h, p.h_kv, S,
-                                                  part);
+                                                  part, pkv);
   return cudaGetLastError();
 }
 
@@ -802,21 +855,48 @@ cudaError_t launch_prefill(const FwdProblem& p, int num_splits, float* part, cud
                            const char** name) {
   cudaError_t e;
   const bool split = num_splits > 1;
+  const PagedKV none{nullptr, nullptr, 0, 0, 0};
   if (p.d == 64) {
-    e = p.bf16 ? launch_t<64, true>(p, num_splits, part, stream)
-               : launch_t<64, false>(p, num_splits, part, stream);
+    e = p.bf16 ? launch_t<64, true, false>(p, num_splits, part, stream, none, nullptr, nullptr)
+               : launch_t<64, false, false>(p, num_splits, part, stream, none, nullptr, nullptr);
     *name = split ? (p.bf16 ? "prefill_splitkv_tcgen05_d64_bf16+decode_combine"
                             : "prefill_splitkv_tcgen05_d64_f16+decode_combine")
                   : (p.bf16 ? "prefill_tcgen05_d64_bf16" : "prefill_tcgen05_d64_f16");
   } else {
-    e = p.bf16 ? launch_t<128, true>(p, num_splits, part, stream)
-               : launch_t<128, false>(p, num_splits, part, stream);
+    e = p.bf16 ? launch_t<128, true, false>(p, num_splits, part, stream, none, nullptr, nullptr)
+               : launch_t<128, false, false>(p, num_splits, part, stream, none, nullptr, nullptr);
     *name = split ? (p.bf16 ? "prefill_splitkv_tcgen05_d128_bf16+decode_combine"
                             : "prefill_splitkv_tcgen05_d128_f16+decode_combine")
                   : (p.bf16 ? "prefill_tcgen05_d128_bf16" : "prefill_tcgen05_d128_f16");
   }
   if (e != cudaSuccess || !split) return e;
   // merge the partials of each query row: rows = B*h*T_q
+  return launch_combine(part, p.o, p.lse, static_cast<long long>(p.B) * p.h * p.T_q, num_splits,
+                        p.d, p.bf16 != 0, stream);
+}
+
+}  // namespace attn
+
+namespace attn {
+
+cudaError_t launch_prefill_paged(const FwdProblem& p, const int* table, const int* lens,
+                                 int page_shift, int max_pages, int num_pages, int num_splits,
+                                 float* part, cudaStream_t stream, const char** name) {
+  const PagedKV pkv{table, lens, page_shift, max_pages, num_pages};
+  cudaError_t e;
+  if (p.d == 64) {
+    e = p.bf16 ? launch_t<64, true, true>(p, num_splits, part, stream, pkv, p.k, p.v)
+               : launch_t<64, false, true>(p, num_splits, part, stream, pkv, p.k, p.v);
+    *name = p.bf16 ? "prefill_paged_tcgen05_d64_bf16+decode_combine"
+                   : "prefill_paged_tcgen05_d64_f16+decode_combine";
+  } else {
+    e = p.bf16 ? launch_t<128, true, true>(p, num_splits, part, stream, pkv, p.k, p.v)
+               : launch_t<128, false, true>(p, num_splits, part, stream, pkv, p.k, p.v);
+    *name = p.bf16 ? "prefill_paged_tcgen05_d128_bf16+decode_combine"
+                   : "prefill_paged_tcgen05_d128_f16+decode_combine";
+  }
+  if (e != cudaSuccess) return e;
+  if (num_splits <= 1) return cudaSuccess;  // the kernel wrote o and lse
   return launch_combine(part, p.o, p.lse, static_cast<long long>(p.B) * p.h * p.T_q, num_splits,
                         p.d, p.bf16 != 0, stream);
 }

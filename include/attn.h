@@ -262,6 +262,10 @@ size_t attn_bwd_workspace_bytes(int B, int h, int T_q, int T_kv, int d);
  * Computational Cost", section "The other shape: one query, many keys");
  * the layout is this library's.
  *
+ * Groups of 4 or more query heads per key/value head with pages of at least
+ * 8 rows run on the tensor cores (each cached row read once for its whole
+ * group); otherwise the CUDA-core kernel reads the cache once per query head.
+ *
  * page_size: a power of two, 1..65536. A length above
  * max_pages_per_seq * page_size is clamped to it; a length <= 0 gives
  * o = 0 and lse = -inf for that sequence. A table entry outside
@@ -284,11 +288,12 @@ attn_status_t attn_fwd_paged_decode(const void* q, const void* k_pages, const vo
 
 /*
  * attn_paged_workspace_bytes -- workspace attn_fwd_paged_decode needs:
- * B*h_q*S*(d+4)*4 bytes, S = num_splits or the library's choice (0 for
- * invalid sizes).
+ * B*h_q*S*(d+4)*4 bytes, S = num_splits or the library's choice (which
+ * depends on the grouping h_q / h_kv), 0 when the call needs none (the
+ * tensor-core path with one partition) or for invalid sizes.
  */
-size_t attn_paged_workspace_bytes(int B, int h_q, int d, int page_size, int max_pages_per_seq,
-                                  int num_splits);
+size_t attn_paged_workspace_bytes(int B, int h_q, int h_kv, int d, int page_size,
+                                  int max_pages_per_seq, int num_splits);
 
 /*
  * attn_fwd_splitkv -- the prefill path (T_q > 1) with the key range of every

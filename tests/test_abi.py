@@ -319,10 +319,13 @@ def test_paged_decode_arguments(L, over, status):
 
 
 def test_paged_workspace_bytes(L):
-    assert _lib.paged_workspace_bytes(2, 4, 64, 16, 8, 5) == 2 * 4 * 5 * 68 * 4
-    assert _lib.paged_workspace_bytes(2, 4, 128, 16, 8, 3) == 2 * 4 * 3 * 132 * 4
-    assert _lib.paged_workspace_bytes(2, 4, 64, 24, 8, 5) == 0
-    assert _lib.paged_workspace_bytes(0, 4, 64, 16, 8, 5) == 0
+    assert _lib.paged_workspace_bytes(2, 4, 2, 64, 16, 8, 5) == 2 * 4 * 5 * 68 * 4
+    assert _lib.paged_workspace_bytes(2, 4, 4, 128, 16, 8, 3) == 2 * 4 * 3 * 132 * 4
+    assert _lib.paged_workspace_bytes(2, 8, 2, 64, 16, 8, 5) == 2 * 8 * 5 * 68 * 4   # tensor cores
+    assert _lib.paged_workspace_bytes(2, 8, 2, 64, 16, 8, 1) == 0   # one partition: none
+    assert _lib.paged_workspace_bytes(2, 4, 2, 64, 24, 8, 5) == 0
+    assert _lib.paged_workspace_bytes(2, 4, 3, 64, 16, 8, 5) == 0
+    assert _lib.paged_workspace_bytes(0, 4, 2, 64, 16, 8, 5) == 0
 
 
 def _splitkv(**over):

@@ -177,7 +177,7 @@ def test_paged_full_size_sampled_rows():
 
 def test_paged_kernel_name_and_workspace():
     q, kp, vp, table, ln = make_paged(2, 4, 2, [100, 50], 128, F16, 16, seed=45)
-    nbytes = _lib.paged_workspace_bytes(2, 4, 128, 16, table.shape[1], 6)
+    nbytes = _lib.paged_workspace_bytes(2, 4, 2, 128, 16, table.shape[1], 6)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     _lib.attn_fwd_paged_decode(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), ln.cuda(),
                                num_splits=6, workspace=ws)
@@ -187,3 +187,36 @@ def test_paged_kernel_name_and_workspace():
         _lib.attn_fwd_paged_decode(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), ln.cuda(),
                                    num_splits=6, workspace=ws[:64])
     assert e.value.status == _lib.ATTN_ERR_WORKSPACE
+
+
+TC_CASES = [
+    # B, h_q, h_kv, lens, d, dtype, page_size, splits -- groups >= 4 with pages
+    # of >= 8 rows: the tensor-core path (K/V tiles gathered through the table)
+    (3, 8, 2, [1000, 1, 517], 64, BF16, 16, 0),
+    (2, 16, 2, [4096, 3000], 128, BF16, 128, 0),
+    (2, 16, 4, [300, 700], 64, F16, 8, 5),          # 8-row pages: 16 boxes per tile
+    (3, 8, 1, [320, 3, 0], 128, BF16, 64, 0),       # a zero-length sequence, group 8
+    (2, 12, 3, [2000, 129], 128, F16, 256, 1),      # one partition: no workspace
+    (1, 32, 2, [16384], 64, BF16, 64, 64),          # group 16, the most partitions
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "x".join(str(x) for x in c[:3]) + f"_ps{c[6]}_s{c[7]}_d{c[4]}")
+def test_paged_decode_tensor_core_path(case):
+    B, hq, hkv, lens, d, dt, ps, splits = case
+    q, kp, vp, table, ln = make_paged(B, hq, hkv, lens, d, dt, ps, seed=46)
+    o, lse = gpu_paged(q, kp, vp, table, ln, splits)
+    assert _lib.last_kernel_name().startswith("prefill_paged_tcgen05")
+    compare_paged(o, lse, oracle_paged(q, kp, vp, table, ln), dt, f"paged tc {case}")
+
+
+def test_paged_tensor_core_bad_table_entry_is_reported():
+    q, kp, vp, table, ln = make_paged(2, 8, 2, [300, 200], 64, BF16, 16, seed=47)
+    bad = table.clone()
+    bad[1, 1] = kp.shape[0] + 3
+    gpu_paged(q, kp, vp, bad, ln, check_status=False)
+    st, word = _lib.get_device_error()
+    assert st == _lib.ATTN_ERR_INVALID_ARG
+    assert (word >> 8) & 0xff == 1          # the prefill kernel's producer
+    o, lse = gpu_paged(q, kp, vp, table, ln)
+    compare_paged(o, lse, oracle_paged(q, kp, vp, table, ln), BF16, "tc after a bad table")
