@@ -180,6 +180,17 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
       : "memory");
 }
 
+// An empty statement tied to registers. The softmax arithmetic is register
+// work, which the compiler may otherwise move across the barrier waits
+// (volatile asm orders only against other volatile asm and memory): the
+// fence keeps the computation of these values before the waits after it.
+__device__ __forceinline__ void reg_fence64f(uint32_t (&r)[64], float& f) {
+#define R8(b) "+r"(r[b]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), "+r"(r[b + 4]), \
+              "+r"(r[b + 5]), "+r"(r[b + 6]), "+r"(r[b + 7])
+  asm volatile("" : R8(0), R8(8), R8(16), R8(24), R8(32), R8(40), R8(48), R8(56), "+f"(f));
+#undef R8
+}
+
 // Bounded wait used only while draining after an error: ignores the
 // status word, gives up after the same time limit.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
@@ -698,6 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
         l += rsa.x + rsa.y;
+        // the exponentials are done here, not after the wait for PV_X below
+        reg_fence64f(pk, l);
 
         if constexpr (C::SEP_P) {
           // P_X and O_X are free once the previous product PV_X finished
