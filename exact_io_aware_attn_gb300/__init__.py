@@ -16,11 +16,13 @@ from ._lib import (  # noqa: F401
     attn_fwd,
     attn_fwd_decode_noalloc,
     attn_fwd_gqa,
+    attn_fwd_host,
     attn_fwd_paged_decode,
     attn_fwd_splitkv,
     decode_num_splits,
     fwd_raw,
     get_device_error,
+    host_buffer_bytes,
     last_kernel_name,
     status_string,
     workspace_bytes,

@@ -52,6 +52,9 @@ SIGNATURES = {
     "attn_fwd_splitkv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP,
                               _SZ, _VP]),
     "attn_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_fwd_host": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ,
+                           _VP]),
+    "attn_host_buffer_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
 }
 
 # Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
@@ -434,4 +437,69 @@ def attn_fwd_splitkv(q, k, v, *, scale=None, causal=False, out=None, lse=None, n
                          wp, wn, _stream_ptr(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def host_buffer_bytes(B, h_q, h_kv, T_q, T_kv, d) -> int:
+    return int(lib().attn_host_buffer_bytes(B, h_q, h_kv, T_q, T_kv, d))
+
+
+def fwd_host_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h_q, h_kv, T_q, T_kv, d, scale, causal,
+                 dtype, buffer_ptr=None, buffer_nbytes=0, stream_ptr=None) -> int:
+    """Direct call of attn_fwd_host (host addresses for q, k, v, o, lse);
+    returns the status code."""
+    return int(lib().attn_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h_q, h_kv, T_q, T_kv, d,
+                                   float(scale), int(causal), int(dtype), buffer_ptr,
+                                   int(buffer_nbytes), stream_ptr))
+
+
+def attn_fwd_host(q, k, v, *, scale=None, causal=False, out=None, lse=None, device_buffer=None,
+                  stream=None, synchronize=True):
+    """The forward on HOST tensors: q [B, h_q, T_q, d], k, v [B, h_kv, T_kv, d]
+    (contiguous CPU tensors of one 16-bit dtype, ideally pinned). The library
+    copies them to the GPU, runs the forward, and copies o and lse back into
+    `out` / `lse` (CPU tensors; allocated pinned if not given). With
+    synchronize=False the call only enqueues the work on the stream and the
+    results are valid after it synchronises. `device_buffer` (a CUDA uint8
+    tensor of at least host_buffer_bytes(...) bytes) holds the device copies;
+    without it they come from the stream-ordered allocator."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CPU tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, h_q, T_q, d = q.shape
+    h_kv, T_kv = k.shape[1], k.shape[2]
+    if k.shape != (B, h_kv, T_kv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, h_kv, T_kv, d] with q's B and d")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, h_q, T_q), dtype=torch.float32).pin_memory()
+    if out.is_cuda or out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU tensor like q")
+    if lse.is_cuda or lse.shape != (B, h_q, T_q) or lse.dtype != torch.float32 or \
+            not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CPU [B, h_q, T_q] tensor")
+    bp, bn = None, 0
+    if device_buffer is not None:
+        if not device_buffer.is_cuda:
+            raise ValueError("device_buffer must be a CUDA tensor")
+        bp, bn = device_buffer.data_ptr(), device_buffer.numel() * device_buffer.element_size()
+    sp = _stream_ptr(stream)
+    st = fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, h_q, h_kv, T_q, T_kv, d, scale, causal, dt, bp, bn, sp)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_host")
+    if synchronize:
+        if stream is None:
+            torch.cuda.current_stream().synchronize()
+        elif not isinstance(stream, int):
+            stream.synchronize()
+        else:
+            torch.cuda.synchronize()
     return out, lse

@@ -546,6 +546,76 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   return run_prefill(p, splits, workspace, workspace_bytes, own, static_cast<cudaStream_t>(stream));
 }
 
+// Device copies of a host-buffer call: q | k | v | o | lse, each at a
+// 256-byte offset. Returns 0 for shapes the forward rejects or an empty one.
+static size_t host_region(int B, int h_q, int h_kv, int T_q, int T_kv, int d, size_t off[5]) {
+  if (B < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || T_q < 1 || T_kv < 1) return 0;
+  if (d != 64 && d != 128) return 0;
+  const size_t qo = static_cast<size_t>(B) * h_q * T_q * d * 2;
+  const size_t kv = static_cast<size_t>(B) * h_kv * T_kv * d * 2;
+  const size_t ls = static_cast<size_t>(B) * h_q * T_q * 4;
+  const size_t sizes[5] = {qo, kv, kv, qo, ls};
+  size_t at = 0;
+  for (int i = 0; i < 5; ++i) {
+    off[i] = at;
+    at += (sizes[i] + 255) & ~static_cast<size_t>(255);
+  }
+  return at;
+}
+
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int h_q, int h_kv, int T_q, int T_kv, int d, float scale,
+                            int causal, int dtype, void* device_buffer,
+                            size_t device_buffer_bytes, void* stream) {
+  if (h_kv < 1) return ATTN_ERR_INVALID_ARG;
+  bool empty = false;
+  attn_status_t st = validate(q, k, v, o, lse, B, h_q, T_q, T_kv, d, scale, causal, dtype, &empty,
+                              h_kv);
+  if (st != ATTN_OK) return st;
+  if (empty) {
+    t_last_kernel = "none";
+    return ATTN_OK;
+  }
+  size_t off[5];
+  const size_t need = host_region(B, h_q, h_kv, T_q, T_kv, d, off);
+  if (need == 0) return ATTN_ERR_INVALID_ARG;
+  const bool own = device_buffer == nullptr && device_buffer_bytes == 0;
+  if (!own && (!device_buffer || device_buffer_bytes < need || !aligned(device_buffer, 16)))
+    return ATTN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(device_buffer);
+  if (own && cudaMallocAsync(reinterpret_cast<void**>(&base), need, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const size_t qo = static_cast<size_t>(B) * h_q * T_q * d * 2;
+  const size_t kv = static_cast<size_t>(B) * h_kv * T_kv * d * 2;
+  const size_t ls = static_cast<size_t>(B) * h_q * T_q * 4;
+  void* dq = base + off[0];
+  void* dk = base + off[1];
+  void* dv = base + off[2];
+  void* dO = base + off[3];
+  float* dl = reinterpret_cast<float*>(base + off[4]);
+  // one copy per tensor, in stream order
+  if (cudaMemcpyAsync(dq, q, qo, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k, kv, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v, kv, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    st = ATTN_ERR_CUDA;
+  } else {
+    st = run(dq, dk, dv, dO, dl, B, h_q, h_kv, T_q, T_kv, d, scale, causal, dtype, 0, nullptr, 0,
+             true, stream);
+    if (st == ATTN_OK &&
+        (cudaMemcpyAsync(o, dO, qo, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+         cudaMemcpyAsync(lse, dl, ls, cudaMemcpyDeviceToHost, s) != cudaSuccess))
+      st = ATTN_ERR_CUDA;
+  }
+  if (own) cudaFreeAsync(base, s);
+  return st;
+}
+
+size_t attn_host_buffer_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int d) {
+  size_t off[5];
+  return host_region(B, h_q, h_kv, T_q, T_kv, d, off);
+}
+
 size_t attn_splitkv_workspace_bytes(int B, int h_q, int T_q, int T_kv, int d, int num_splits) {
   if (B < 1 || h_q < 1 || T_q < 2 || T_kv < 1 || (d != 64 && d != 128)) return 0;
   if (num_splits < 0 || num_splits > 64) return 0;

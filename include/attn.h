@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 typedef enum {
   ATTN_OK = 0,
@@ -152,6 +152,42 @@ size_t attn_workspace_bytes(int B, int h, int T_q, int T_kv, int d, int num_spli
  * invalid). Deterministic for a given device.
  */
 int attn_decode_num_splits(int B, int h, int T_kv, int d);
+
+/*
+ * attn_fwd_host -- the forward with q, k, v, o and lse in HOST memory. The
+ * path the pages describe starts and ends in HBM ("FlashAttention IO-aware
+ * tiling lab", "Attention memory path": HBM to on-chip memory to the tensor
+ * cores and back to HBM); this entry adds the level below it, the host, as a
+ * convenience for callers whose tensors live there: the kernels are the
+ * same. Shapes, dtype, scale, causal and the grouped-query heads as in
+ * attn_fwd_gqa (h_kv == h_q: plain attention). In stream order on `stream`
+ * the library copies q, k and v to device memory (one cudaMemcpyAsync each),
+ * runs the same kernels as attn_fwd, and copies o and lse back. It returns
+ * once the work is enqueued: o and lse hold the result after `stream` is
+ * synchronised. Host buffers should be page-locked (cudaHostAlloc or
+ * cudaHostRegister) for the copies to run asynchronously; with pageable
+ * buffers the driver may stage the copies and block the calling thread.
+ *   device_buffer  device memory for the device copies, 16-byte aligned, at
+ *                  least attn_host_buffer_bytes(...) bytes, owned by the caller
+ *                  and kept allocated until the work completes; NULL with
+ *                  device_buffer_bytes 0: taken from and returned to the
+ *                  stream-ordered allocator (cudaMallocAsync/cudaFreeAsync).
+ * The decode path's workspace is taken from the stream-ordered allocator.
+ * Returns ATTN_ERR_WORKSPACE if a caller buffer is too small or misaligned,
+ * otherwise the errors of attn_fwd_gqa (host pointers are checked for NULL,
+ * alignment and overlap like device pointers).
+ */
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int h_q, int h_kv, int T_q, int T_kv, int d, float scale,
+                            int causal, int dtype, void* device_buffer,
+                            size_t device_buffer_bytes, void* stream);
+
+/*
+ * attn_host_buffer_bytes -- device bytes attn_fwd_host needs for the copies
+ * of q, k, v, o and lse (each at a 256-byte offset); 0 for an invalid or
+ * empty shape.
+ */
+size_t attn_host_buffer_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int d);
 
 /*
  * attn_get_device_error -- synchronises `stream`, then reads and clears the

@@ -357,3 +357,42 @@ def test_splitkv_workspace_bytes(L):
     assert _lib.splitkv_workspace_bytes(1, 4, 256, 4096, 64, 8) == 4 * 256 * 8 * 68 * 4
     assert _lib.splitkv_workspace_bytes(1, 4, 256, 4096, 64, 1) == 0
     assert _lib.splitkv_workspace_bytes(1, 4, 1, 4096, 64, 8) == 0
+
+
+def _host(**over):
+    a = dict(B=1, h_q=4, h_kv=2, T_q=256, T_kv=1024, d=64, scale=0.125, causal=1,
+             dtype=_lib.ATTN_BF16)
+    buf, nbytes = over.pop("buf", WS), over.pop("nbytes", 64)
+    a.update(over)
+    return _lib.fwd_host_raw(Q, K, V, O, LSE, a["B"], a["h_q"], a["h_kv"], a["T_q"], a["T_kv"],
+                             a["d"], a["scale"], a["causal"], a["dtype"], buf, nbytes, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(h_kv=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(h_kv=3), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=7), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(T_q=2000), _lib.ATTN_ERR_INVALID_ARG),          # causal needs T_q <= T_kv
+    (dict(), _lib.ATTN_ERR_WORKSPACE),                    # 64 bytes: far too small
+    (dict(buf=None, nbytes=1 << 30), _lib.ATTN_ERR_WORKSPACE),
+    (dict(buf=WS + 8, nbytes=1 << 30), _lib.ATTN_ERR_WORKSPACE),  # misaligned
+    (dict(B=0), _lib.ATTN_OK),
+])
+def test_host_entry_arguments(L, over, status):
+    """attn_fwd_host checks its host pointers and the device buffer before
+    the first copy is enqueued."""
+    assert _host(**over) == status
+
+
+def test_host_buffer_bytes(L):
+    # q, k, v, o, lse each at a 256-byte offset
+    qo = 1 * 4 * 256 * 64 * 2
+    kv = 1 * 2 * 1024 * 64 * 2
+    ls = 1 * 4 * 256 * 4
+    assert _lib.host_buffer_bytes(1, 4, 2, 256, 1024, 64) == 2 * qo + 2 * kv + ls
+    assert _lib.host_buffer_bytes(1, 4, 2, 1, 1000, 128) == (
+        2 * ((4 * 128 * 2 + 255) // 256 * 256) + 2 * (2 * 1000 * 128 * 2) + 256)
+    assert _lib.host_buffer_bytes(1, 4, 3, 256, 1024, 64) == 0   # h_q not a multiple of h_kv
+    assert _lib.host_buffer_bytes(0, 4, 2, 256, 1024, 64) == 0
+    assert _lib.host_buffer_bytes(1, 4, 2, 256, 1024, 96) == 0
