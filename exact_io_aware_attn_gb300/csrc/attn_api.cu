@@ -199,9 +199,16 @@ bool paged_on_tensor_cores(int h_q, int h_kv, int page_size) {
   return gqa_decode_on_tensor_cores(h_q, h_kv) && page_size >= 8;
 }
 
+// Tensor-core forward units per key partition and query-tile pair: B*h
+// heads, or head pairs in head-pair mode (attn_internal.h).
+long long tc_units(int B, int h, int T_q, int d) {
+  const long long bh = static_cast<long long>(B) * h;
+  return attn::head_pair_mode(d, T_q, bh) ? (bh + 1) / 2 : bh;
+}
+
 int auto_splits(int B, int h, int h_kv, int T_kv, int d) {
-  if (gqa_decode_on_tensor_cores(h, h_kv))  // one prefill CTA per SM
-    return std::min(64, attn::detail::choose_splits_cap(static_cast<long long>(B) * h_kv, T_kv,
+  if (gqa_decode_on_tensor_cores(h, h_kv))  // one prefill CTA per SM, per unit of heads
+    return std::min(64, attn::detail::choose_splits_cap(tc_units(B, h_kv, h / h_kv, d), T_kv,
                                                         sm_count()));
   return choose_splits(decode_rows(B, h, h_kv), T_kv, d, attn::decode_heads_per_cta(h / h_kv));
 }
@@ -209,9 +216,9 @@ int auto_splits(int B, int h, int h_kv, int T_kv, int d) {
 // Prefill key partitions: only when the (query-tile pair, head) units fill
 // less than half the SMs; then enough partitions to reach about one unit per
 // SM, at least 2 key tiles each, at most 64.
-int prefill_auto_splits(int B, int h, int T_q, int T_kv) {
+int prefill_auto_splits(int B, int h, int T_q, int T_kv, int d) {
   const long long pairs = ((static_cast<long long>(T_q) + 127) / 128 + 1) / 2;
-  const long long units = pairs * B * h;
+  const long long units = tc_units(B, h, T_q, d) * pairs;
   const long long sms = sm_count();
   if (units * 2 > sms) return 1;
   const long long n_kv = (static_cast<long long>(T_kv) + 127) / 128;
@@ -283,7 +290,7 @@ attn_status_t run(const void* q, const void* k, const void* v, void* o, float* l
     // attn_fwd (own workspace) cuts the key range of small problems into
     // partitions; attn_fwd_ex and attn_fwd_gqa with a caller workspace keep
     // the prefill unsplit (their workspace contract is decode-only)
-    const int splits = own_workspace ? prefill_auto_splits(B, h, T_q, T_kv) : 1;
+    const int splits = own_workspace ? prefill_auto_splits(B, h, T_q, T_kv, d) : 1;
     return run_prefill(p, splits, nullptr, 0, true, s);
   }
   // the same choice attn_workspace_bytes(..., 0) reports (occupancy of the bf16
@@ -541,7 +548,7 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   }
   attn::FwdProblem p{q, k, v, o, lse, B, h_q, T_q, T_kv, d, scale, causal,
                      dtype == ATTN_BF16 ? 1 : 0, nullptr, h_kv};
-  const int splits = num_splits > 0 ? num_splits : prefill_auto_splits(B, h_q, T_q, T_kv);
+  const int splits = num_splits > 0 ? num_splits : prefill_auto_splits(B, h_q, T_q, T_kv, d);
   const bool own = workspace == nullptr && workspace_bytes == 0;
   return run_prefill(p, splits, workspace, workspace_bytes, own, static_cast<cudaStream_t>(stream));
 }
@@ -619,7 +626,7 @@ size_t attn_host_buffer_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int d
 size_t attn_splitkv_workspace_bytes(int B, int h_q, int T_q, int T_kv, int d, int num_splits) {
   if (B < 1 || h_q < 1 || T_q < 2 || T_kv < 1 || (d != 64 && d != 128)) return 0;
   if (num_splits < 0 || num_splits > 64) return 0;
-  const int splits = num_splits > 0 ? num_splits : prefill_auto_splits(B, h_q, T_q, T_kv);
+  const int splits = num_splits > 0 ? num_splits : prefill_auto_splits(B, h_q, T_q, T_kv, d);
   return prefill_ws_bytes(B, h_q, T_q, d, splits);
 }
 

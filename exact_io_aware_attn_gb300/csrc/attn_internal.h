@@ -105,6 +105,13 @@ int decode_paged_ctas_per_sm(int d);
 // per key/value head decode on the tensor cores instead (attn_api.cu).
 inline int decode_heads_per_cta(int group) { return (group % 2 == 0) ? 2 : 1; }
 
+// The tensor-core forward pairs two heads per work unit (each with its own
+// query tile and key/value stream) when a head has at most 128 query rows at
+// d = 64, so that both tiles of a unit exist; its units are then
+// ceil(B*h / 2) per key partition instead of B*h. (Contiguous K/V only: the
+// paged mode keeps one head per unit.)
+inline bool head_pair_mode(int d, int T_q, long long BH) { return d == 64 && T_q <= 128 && BH >= 2; }
+
 // Split kernel occupancy (CTAs per SM) for the split-count heuristic.
 int decode_split_ctas_per_sm(int d, int heads_per_cta);
 

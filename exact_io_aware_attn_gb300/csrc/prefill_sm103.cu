@@ -201,12 +201,19 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// One work unit: query tiles A = rows [q0, q0+128) and B = [q0+128, q0+256)
-// of head bh, key partition s of S: key tiles [j0, j0 + n_all), of which tile
-// A sees the first n_a and tile B the first n_b (causal: up to the diagonal).
-// With S = 1 the partition is every key tile the pair sees.
+// One work unit: query tiles A and B and key partition s of S: key tiles
+// [j0, j0 + n_all), of which tile A sees the first n_a and tile B the first
+// n_b (causal: up to the diagonal). Row-pair mode: A = rows [q0, q0+128) and
+// B = [q0+128, q0+256) of one head, reading one K/V stream. Head-pair mode
+// (at most 128 query rows, d = 64): A = the rows of head bh and B = those of
+// head bh + 1, each reading its own K/V stream, so that the two tiles that
+// keep the tensor core and the softmax warps busy in turn both exist for
+// short queries (grouped-query decode, short prefill); rows_b = 0 when bh is
+// the last head. With S = 1 the partition is every key tile the tiles see.
 struct Unit {
-  int bh, kvbh, q0, rows_b, n_a, n_b, n_all, j0, s, tkv;
+  int bh, kvbh, q0, tkv;          // tile A: head, key/value head, first row, keys
+  int bh_b, kvbh_b, q0_b, tkv_b;  // tile B
+  int rows_b, n_a, n_b, n_all, j0, s;
 };
 
 // Keys from a paged pool ([num_pages][h_kv][page_size][d]) through a block
@@ -219,34 +226,46 @@ struct PagedKV {
   int page_shift, max_pages, num_pages;
 };
 
+template <bool HP>
 __device__ __forceinline__ Unit unit_info(int u, int BH, int n_pairs, int T_q, int T_kv,
-                                          int causal, int h_q, int h_kv, int S,
-                                          const int* lens = nullptr) {
+                                          int causal, int h_q, int h_kv, int S, const int* lens) {
   Unit w;
   w.s = u % S;
   u /= S;
-  const int pair = n_pairs - 1 - u / BH;  // heaviest pairs first under a causal mask
-  w.bh = u % BH;
-  // paged mode: this sequence's length (b = bh / h_q), clamped to what its
-  // table can name (T_kv); otherwise every head has T_kv keys
-  w.tkv = lens ? max(0, min(__ldg(lens + w.bh / h_q), T_kv)) : T_kv;
-  T_kv = w.tkv;
+  // paged mode: a sequence's length (b = bh / h_q), clamped to what its table
+  // can name (T_kv); otherwise every head has T_kv keys
+  auto keys_of = [&](int bh) { return lens ? max(0, min(__ldg(lens + bh / h_q), T_kv)) : T_kv; };
   // grouped-query attention: query head i reads key/value head i / (h_q / h_kv)
-  w.kvbh = (w.bh / h_q) * h_kv + (w.bh % h_q) / (h_q / h_kv);
-  w.q0 = pair * 2 * kBM;
-  const int rows_a = min(kBM, T_q - w.q0);
-  w.rows_b = max(0, min(kBM, T_q - w.q0 - kBM));
-  const int n_kv = (T_kv + kBN - 1) / kBN;
-  const int off = T_kv - T_q;
-  const int last_a = w.q0 + rows_a - 1;
-  w.n_a = causal ? min(n_kv, (last_a + off + kBN) / kBN) : n_kv;
-  if (w.rows_b > 0) {
-    const int last_b = w.q0 + kBM + w.rows_b - 1;
-    w.n_b = causal ? min(n_kv, (last_b + off + kBN) / kBN) : n_kv;
+  auto kv_of = [&](int bh) { return (bh / h_q) * h_kv + (bh % h_q) / (h_q / h_kv); };
+  int rows_a;
+  if constexpr (HP) {
+    w.bh = 2 * u;
+    w.bh_b = w.bh + 1;
+    w.q0 = 0;
+    w.q0_b = 0;
+    rows_a = T_q;
+    w.rows_b = w.bh_b < BH ? T_q : 0;
   } else {
-    w.n_b = 0;
+    const int pair = n_pairs - 1 - u / BH;  // heaviest pairs first under a causal mask
+    w.bh = u % BH;
+    w.bh_b = w.bh;
+    w.q0 = pair * 2 * kBM;
+    w.q0_b = w.q0 + kBM;
+    rows_a = min(kBM, T_q - w.q0);
+    w.rows_b = max(0, min(kBM, T_q - w.q0_b));
   }
-  // key partition s of S: ceil(N/S) key tiles each, N = the pair's key tiles
+  w.tkv = keys_of(w.bh);
+  w.kvbh = kv_of(w.bh);
+  w.tkv_b = HP && w.rows_b > 0 ? keys_of(w.bh_b) : w.tkv;
+  w.kvbh_b = HP && w.rows_b > 0 ? kv_of(w.bh_b) : w.kvbh;
+  const int off = T_kv - T_q;  // causal alignment (the paged mode is never causal)
+  auto n_tiles = [&](int keys, int last_row) {
+    const int n_kv = (keys + kBN - 1) / kBN;
+    return causal ? min(n_kv, (last_row + off + kBN) / kBN) : n_kv;
+  };
+  w.n_a = n_tiles(w.tkv, w.q0 + rows_a - 1);
+  w.n_b = w.rows_b > 0 ? n_tiles(w.tkv_b, w.q0_b + w.rows_b - 1) : 0;
+  // key partition s of S: ceil(N/S) key tiles each, N = the unit's key tiles
   const int n_full = max(w.n_a, w.n_b);
   const int chunk = (n_full + S - 1) / S;
   w.j0 = w.s * chunk;
@@ -264,13 +283,15 @@ __device__ __forceinline__ int unit_of_round(int r, int bid, int G) {
   return (r & 1) ? r * G + (G - 1 - bid) : r * G + bid;
 }
 
-template <int D, bool BF16, bool PAGED>
+// HP: head-pair mode (two heads per unit, contiguous K/V, d = 64 only).
+template <int D, bool BF16, bool PAGED, bool HP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, void* __restrict__ out,
                    float* __restrict__ lse, int T_q, int T_kv, int BH, int n_pairs,
                    float scale_log2, int causal, unsigned int* __restrict__ status, int h_q,
                    int h_kv, int S, float* __restrict__ part, const PagedKV pkv) {
+  static_assert(!HP || (D == 64 && !PAGED), "head pairs: d = 64, contiguous K/V");
   using C = Cfg<D>;
   constexpr int SL = C::SLOTS;
   extern __shared__ uint8_t smem_raw[];
@@ -292,9 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // units: (query-tile pair, head, key partition); S > 1 writes fp32
-  // partials (o, m, l) to `part` for the merge kernel instead of O and lse
-  const int U = n_pairs * BH * S;
+  // units: (query-tile pair, head, key partition), or (head pair, key
+  // partition) in head-pair mode; S > 1 writes fp32 partials (o, m, l) to
+  // `part` for the merge kernel instead of O and lse
+  const int U = (HP ? (BH + 1) / 2 : n_pairs * BH) * S;
   const int G = static_cast<int>(gridDim.x);
   const int bid = static_cast<int>(blockIdx.x);
   const int off = T_kv - T_q;
@@ -348,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
+          const Unit w = unit_info<HP>(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
           if (w.n_all == 0) continue;  // a key partition the pair does not reach
           ok = ptx::mbar_wait(q_empty, (nq & 1) ^ 1, status, status_word(kKernPrefill, kSiteProdQ));
           if (!ok) break;
@@ -358,51 +380,85 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_load_3d(smem + C::OFF_Q + c * kSub, &tmQ, q_full, c * 64, w.q0, w.bh, pol_q);
             if (w.rows_b > 0)
               ptx::tma_load_3d(smem + C::OFF_Q + C::TILE_BYTES + c * kSub, &tmQ, q_full, c * 64,
-                               w.q0 + kBM, w.bh, pol_q);
+                               w.q0_b, w.bh_b, pol_q);
           }
           ++nq;
-          for (int j = 0; ok && j < w.n_all; ++j) {
+          if constexpr (!HP) {
+            // one stream for both tiles: K_j, V_j
+            for (int j = 0; ok && j < w.n_all; ++j) {
 #pragma unroll
-            for (int kind = 0; kind < 2; ++kind) {  // K_j, then V_j
-              const uint32_t slot = g % SL;
-              ok = ptx::mbar_wait(&slot_empty[slot], ((g / SL) & 1) ^ 1, status,
-                                  status_word(kKernPrefill, kSiteProdSlot));
-              if (!ok) break;
-              ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
-              uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
-              if constexpr (PAGED) {
-                // the tile's 128 keys in boxes of min(page_size, 128) rows, each
-                // from the page the table names (rows past the length: page 0,
-                // masked later; a bad entry is reported, never dereferenced)
-                const int rows = min(1 << pkv.page_shift, kBN);
-                const int b = w.bh / h_q;  // sequence of this virtual head
-                const int kvh = w.bh - b * h_q;
-                for (int i = 0; i < kBN; i += rows) {
-                  const int key = (w.j0 + j) * kBN + i;
-                  int pg = 0;
-                  if (key < w.tkv) {
-                    pg = __ldg(pkv.table + static_cast<size_t>(b) * pkv.max_pages +
-                               (key >> pkv.page_shift));
-                    if (static_cast<unsigned>(pg) >= static_cast<unsigned>(pkv.num_pages)) {
-                      atomicCAS(status, 0u,
-                                status_word_code(1u /* ATTN_ERR_INVALID_ARG */, kKernPrefill,
-                                                 kSiteBadPage));
-                      pg = 0;
+              for (int kind = 0; kind < 2; ++kind) {  // K_j, then V_j
+                const uint32_t slot = g % SL;
+                ok = ptx::mbar_wait(&slot_empty[slot], ((g / SL) & 1) ^ 1, status,
+                                    status_word(kKernPrefill, kSiteProdSlot));
+                if (!ok) break;
+                ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
+                uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+                if constexpr (PAGED) {
+                  // the tile's 128 keys in boxes of min(page_size, 128) rows, each
+                  // from the page the table names (rows past the length: page 0,
+                  // masked later; a bad entry is reported, never dereferenced)
+                  const int rows = min(1 << pkv.page_shift, kBN);
+                  const int b = w.bh / h_q;  // sequence of this virtual head
+                  const int kvh = w.bh - b * h_q;
+                  for (int i = 0; i < kBN; i += rows) {
+                    const int key = (w.j0 + j) * kBN + i;
+                    int pg = 0;
+                    if (key < w.tkv) {
+                      pg = __ldg(pkv.table + static_cast<size_t>(b) * pkv.max_pages +
+                                 (key >> pkv.page_shift));
+                      if (static_cast<unsigned>(pg) >= static_cast<unsigned>(pkv.num_pages)) {
+                        atomicCAS(status, 0u,
+                                  status_word_code(1u /* ATTN_ERR_INVALID_ARG */, kKernPrefill,
+                                                   kSiteBadPage));
+                        pg = 0;
+                      }
                     }
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                      ptx::tma_load_3d(dst + c * kSub + i * 128, kind ? &tmV : &tmK,
+                                       &slot_full[slot], c * 64, key & ((1 << pkv.page_shift) - 1),
+                                       pg * h_q + kvh, pol_kv);
                   }
+                } else {
 #pragma unroll
                   for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d(dst + c * kSub + i * 128, kind ? &tmV : &tmK,
-                                     &slot_full[slot], c * 64, key & ((1 << pkv.page_shift) - 1),
-                                     pg * h_q + kvh, pol_kv);
+                    ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot], c * 64,
+                                     (w.j0 + j) * kBN, w.kvbh, pol_kv);
                 }
-              } else {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                  ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot], c * 64,
-                                   (w.j0 + j) * kBN, w.kvbh, pol_kv);
+                ++g;
               }
-              ++g;
+            }
+          } else {
+            // a stream per tile: K_j of A, K_j of B, V_j of A, V_j of B. Each
+            // slot is read by one tile; this thread stands in for the release
+            // of the other (slot_empty counts two), and for both when the
+            // tile it belongs to has no key tile j (then the slot gets no data
+            // and its full barrier just completes, keeping the phases in step).
+            const int nt = w.rows_b > 0 ? 2 : 1;
+            for (int j = 0; ok && j < w.n_all; ++j) {
+              for (int kind = 0; ok && kind < 2; ++kind) {
+                for (int t = 0; ok && t < nt; ++t) {
+                  const uint32_t slot = g % SL;
+                  ok = ptx::mbar_wait(&slot_empty[slot], ((g / SL) & 1) ^ 1, status,
+                                      status_word(kKernPrefill, kSiteProdSlot));
+                  if (!ok) break;
+                  const bool skip = j >= (t ? w.n_b : w.n_a);
+                  if (skip) {
+                    ptx::mbar_arrive(&slot_full[slot]);
+                    ptx::mbar_arrive(&slot_empty[slot]);
+                  } else {
+                    ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
+                    uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                      ptx::tma_load_3d(dst + c * kSub, kind ? &tmV : &tmK, &slot_full[slot],
+                                       c * 64, (w.j0 + j) * kBN, t ? w.kvbh_b : w.kvbh, pol_kv);
+                  }
+                  ptx::mbar_arrive(&slot_empty[slot]);
+                  ++g;
+                }
+              }
             }
           }
         }
@@ -517,12 +573,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
+          const Unit w = unit_info<HP>(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
           if (w.n_all == 0) continue;  // skipped by the producer too
           const int n_x = x ? w.n_b : w.n_a;
           ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
           ++nq;
           if (!ok) break;
+          if constexpr (HP) {
+            // this tile's own slots: per key tile the ring holds K_A, K_B,
+            // V_A, V_B (K_A, V_A when there is no tile B); the producer
+            // stands in for the other tile's releases and for key tiles this
+            // tile does not see
+            const uint32_t per = w.rows_b > 0 ? 4u : 2u;
+            const uint32_t kx = g + static_cast<uint32_t>(x);         // K_0 of this tile
+            const uint32_t vx = kx + per / 2;                         // V_0 of this tile
+            if (n_x == 0) {
+              commit(q_empty);  // no score product of this tile reads Q
+            } else {
+              ok = wait_slot(kx);
+              if (!ok) break;
+              ptx::tc_fence_after();
+              ok = issue_s_sep(x, kx % SL);
+              if (!ok) break;
+              commit(&slot_empty[kx % SL]);
+              if (n_x == 1) commit(q_empty);
+            }
+            for (int j = 0; j < n_x; ++j) {
+              const uint32_t vi = vx + per * j;        // V_j
+              const uint32_t ki = kx + per * (j + 1);  // K_{j+1}
+              if (j + 1 < n_x) {
+                ok = wait_slot(ki);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                ok = issue_s_sep(x, ki % SL);
+                if (!ok) break;
+                commit(&slot_empty[ki % SL]);
+                if (j + 2 == n_x) commit(q_empty);
+              }
+              ok = wait_slot(vi);
+              if (!ok) break;
+              ok = wait_p(x, j == 0);
+              if (!ok) break;
+              issue_pv_sep(x, vi % SL, j == 0);
+              if (j == n_x - 1) commit(&o_full[x]);
+              commit(&slot_empty[vi % SL]);
+            }
+            g += per * w.n_all;
+            continue;
+          }
           ok = wait_slot(g);  // K_0
           if (!ok) break;
           ptx::tc_fence_after();
@@ -560,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; ok && r * G < U; ++r) {
           const int u = unit_of_round(r, bid, G);
           if (u >= U) continue;
-          const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
+          const Unit w = unit_info<HP>(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
           if (w.n_all == 0) continue;  // skipped by the producer too
           ok = wait_bar(q_full, nq & 1, kSiteMmaQ);
           ++nq;
@@ -628,21 +726,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; ok && rr * G < U; ++rr) {
       const int u = unit_of_round(rr, bid, G);
       if (u >= U) continue;
-      const Unit w = unit_info(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
+      const Unit w = unit_info<HP>(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
       const int n_x = x ? w.n_b : w.n_a;
-      const int row = w.q0 + x * kBM + r;        // absolute query row
+      const int bh_x = HP && x ? w.bh_b : w.bh;      // this tile's head
+      const int row = (HP ? 0 : w.q0 + x * kBM) + r;  // absolute query row
       if (n_x == 0) {
         // no key of this partition for this tile: an empty partial (weight 0
-        // in the merge) for each of its rows
-        if (S > 1 && row < T_q && (x == 0 || w.rows_b > 0)) {
-          float* pr = part + ((static_cast<size_t>(w.bh) * T_q + row) * S + w.s) * (D + 4);
+        // in the merge) for each of its rows; unsplit (a sequence of length 0
+        // in the paged mode), the output of a row with no keys: o = 0,
+        // lse = -inf
+        if (row < T_q && (x == 0 || w.rows_b > 0)) {
+          if (S > 1) {
+            float* pr = part + ((static_cast<size_t>(bh_x) * T_q + row) * S + w.s) * (D + 4);
 #pragma unroll
-          for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(pr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(pr + D) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(pr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(pr + D) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+          } else if constexpr (PAGED) {
+            // (only a paged sequence can have no keys at all)
+            uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) +
+                                                   (static_cast<size_t>(bh_x) * T_q + row) * D * 2);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+            lse[static_cast<size_t>(bh_x) * T_q + row] = -INFINITY;
+          }
         }
         continue;
       }
-      const int last_key = causal ? min(w.tkv - 1, row + off) : w.tkv - 1;
+      const int tkv_x = HP && x ? w.tkv_b : w.tkv;
+      const int last_key = causal ? min(tkv_x - 1, row + off) : tkv_x - 1;
       float m_used = -INFINITY;  // reference max, log2 units of the scaled score
       float l = 0.f;
 
@@ -759,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (S > 1) {
         // partial of key partition s: unnormalised o, and (m, l) in log2
         // units of the scaled score -- the decode partial format
-        float* pr = part + ((static_cast<size_t>(w.bh) * T_q + (write ? row : 0)) * S + w.s) * (D + 4);
+        float* pr = part + ((static_cast<size_t>(bh_x) * T_q + (write ? row : 0)) * S + w.s) * (D + 4);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t raw[32];
@@ -780,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv_l = 1.f / l;
       uint8_t* orow = reinterpret_cast<uint8_t*>(out) +
-                      (static_cast<size_t>(w.bh) * T_q + (write ? row : 0)) * D * 2;
+                      (static_cast<size_t>(bh_x) * T_q + (write ? row : 0)) * D * 2;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t raw[32];
@@ -800,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (write)
-        lse[static_cast<size_t>(w.bh) * T_q + row] = (m_used + __log2f(l)) * 0.69314718055994531f;
+        lse[static_cast<size_t>(bh_x) * T_q + row] = (m_used + __log2f(l)) * 0.69314718055994531f;
       ptx::tc_fence_before();
       ptx::mbar_arrive(&o_empty[x]);
     }
@@ -817,11 +928,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool PAGED>
+template <int D, bool BF16, bool PAGED, bool HP>
 cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t stream,
                      const PagedKV& pkv, const void* k_pool, const void* v_pool) {
   using C = Cfg<D>;
-  auto kern = prefill_kernel<D, BF16, PAGED>;
+  auto kern = prefill_kernel<D, BF16, PAGED, HP>;
   static std::mutex mu;
   static uint64_t configured = 0;  // one bit per device ordinal
   int dev = 0;
@@ -852,7 +963,8 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t strea
   }
   const int n_qtiles = (p.T_q + kBM - 1) / kBM;
   const int n_pairs = (n_qtiles + 1) / 2;
-  const long long units = static_cast<long long>(n_pairs) * BH * S;
+  const long long units =
+      static_cast<long long>(HP ? (BH + 1) / 2 : static_cast<long long>(n_pairs) * BH) * S;
   const int sms = device_sms(dev);
   const int grid = static_cast<int>(units < sms ? units : sms);
   const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
@@ -870,14 +982,21 @@ cudaError_t launch_prefill(const FwdProblem& p, int num_splits, float* part, cud
   const bool split = num_splits > 1;
   const PagedKV none{nullptr, nullptr, 0, 0, 0};
   if (p.d == 64) {
-    e = p.bf16 ? launch_t<64, true, false>(p, num_splits, part, stream, none, nullptr, nullptr)
-               : launch_t<64, false, false>(p, num_splits, part, stream, none, nullptr, nullptr);
+    // short queries: two heads per unit (head-pair mode); not with a paged
+    // cache, whose one producer thread would then make twice the page-table
+    // lookups per key tile (measured slower)
+    if (head_pair_mode(64, p.T_q, static_cast<long long>(p.B) * p.h))
+      e = p.bf16 ? launch_t<64, true, false, true>(p, num_splits, part, stream, none, nullptr, nullptr)
+                 : launch_t<64, false, false, true>(p, num_splits, part, stream, none, nullptr, nullptr);
+    else
+      e = p.bf16 ? launch_t<64, true, false, false>(p, num_splits, part, stream, none, nullptr, nullptr)
+                 : launch_t<64, false, false, false>(p, num_splits, part, stream, none, nullptr, nullptr);
     *name = split ? (p.bf16 ? "prefill_splitkv_tcgen05_d64_bf16+decode_combine"
                             : "prefill_splitkv_tcgen05_d64_f16+decode_combine")
                   : (p.bf16 ? "prefill_tcgen05_d64_bf16" : "prefill_tcgen05_d64_f16");
   } else {
-    e = p.bf16 ? launch_t<128, true, false>(p, num_splits, part, stream, none, nullptr, nullptr)
-               : launch_t<128, false, false>(p, num_splits, part, stream, none, nullptr, nullptr);
+    e = p.bf16 ? launch_t<128, true, false, false>(p, num_splits, part, stream, none, nullptr, nullptr)
+               : launch_t<128, false, false, false>(p, num_splits, part, stream, none, nullptr, nullptr);
     *name = split ? (p.bf16 ? "prefill_splitkv_tcgen05_d128_bf16+decode_combine"
                             : "prefill_splitkv_tcgen05_d128_f16+decode_combine")
                   : (p.bf16 ? "prefill_tcgen05_d128_bf16" : "prefill_tcgen05_d128_f16");
@@ -898,13 +1017,13 @@ cudaError_t launch_prefill_paged(const FwdProblem& p, const int* table, const in
   const PagedKV pkv{table, lens, page_shift, max_pages, num_pages};
   cudaError_t e;
   if (p.d == 64) {
-    e = p.bf16 ? launch_t<64, true, true>(p, num_splits, part, stream, pkv, p.k, p.v)
-               : launch_t<64, false, true>(p, num_splits, part, stream, pkv, p.k, p.v);
+    e = p.bf16 ? launch_t<64, true, true, false>(p, num_splits, part, stream, pkv, p.k, p.v)
+               : launch_t<64, false, true, false>(p, num_splits, part, stream, pkv, p.k, p.v);
     *name = p.bf16 ? "prefill_paged_tcgen05_d64_bf16+decode_combine"
                    : "prefill_paged_tcgen05_d64_f16+decode_combine";
   } else {
-    e = p.bf16 ? launch_t<128, true, true>(p, num_splits, part, stream, pkv, p.k, p.v)
-               : launch_t<128, false, true>(p, num_splits, part, stream, pkv, p.k, p.v);
+    e = p.bf16 ? launch_t<128, true, true, false>(p, num_splits, part, stream, pkv, p.k, p.v)
+               : launch_t<128, false, true, false>(p, num_splits, part, stream, pkv, p.k, p.v);
     *name = p.bf16 ? "prefill_paged_tcgen05_d128_bf16+decode_combine"
                    : "prefill_paged_tcgen05_d128_f16+decode_combine";
   }

@@ -84,7 +84,10 @@ DECODE_GQA = Workload("decode_gqa_B32_hq32_hkv8_Tkv16384_d128_bf16", 32, 32, 1, 
 # pair leaves most SMs idle and the key range is split.
 CHUNKED_PREFILL = Workload("chunked_prefill_B1_h8_Tq256_Tkv16384_d128_bf16", 1, 8, 256, 16384, 128,
                            BF16, True)
-EXTRA_WORKLOADS = [DECODE_GQA, CHUNKED_PREFILL]
+# The same grouped-query decode at d = 64 (half the bytes per key row).
+DECODE_GQA_D64 = Workload("decode_gqa_B32_hq32_hkv8_Tkv16384_d64_bf16", 32, 32, 1, 16384, 64, BF16,
+                          False, h_kv=8)
+EXTRA_WORKLOADS = [DECODE_GQA, DECODE_GQA_D64, CHUNKED_PREFILL]
 
 
 def make_qkv(B, h, T_q, T_kv, d, dtype=BF16, mult=1.0, seed=0, device="cpu", h_kv=None):

@@ -71,6 +71,9 @@ def test_gqa_decode_full_size():
     (1, 16, 1, 129, 128, F16, 1),       # group 16, one partition: the plain kernel writes o
     (3, 8, 2, 1, 64, BF16, 0),          # a single key
     (1, 32, 8, 16384, 128, BF16, 64),   # the most partitions
+    (3, 8, 1, 1000, 64, BF16, 0),       # three key/value heads: two in a unit, one alone
+    (1, 4, 1, 500, 64, F16, 1),         # one key/value head: no pair, one partition
+    (5, 4, 1, 2500, 64, BF16, 9),       # pairs across sequences, nine partitions
 ])
 def test_gqa_decode_tensor_core_path(shape):
     B, hq, hkv, tk, d, dt, splits = shape

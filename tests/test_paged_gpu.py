@@ -198,6 +198,11 @@ TC_CASES = [
     (3, 8, 1, [320, 3, 0], 128, BF16, 64, 0),       # a zero-length sequence, group 8
     (2, 12, 3, [2000, 129], 128, F16, 256, 1),      # one partition: no workspace
     (1, 32, 2, [16384], 64, BF16, 64, 64),          # group 16, the most partitions
+    # one key/value head at d = 64: the two heads of a unit come from
+    # different sequences (different lengths), the last unit has one head
+    (3, 4, 1, [1000, 7, 517], 64, BF16, 16, 0),
+    (3, 4, 1, [300, 0, 50], 64, BF16, 16, 1),       # length 0, one partition: o = 0
+    (4, 8, 1, [0, 2000, 64, 900], 64, F16, 8, 0),   # length 0 in a unit's first head
 ]
 
 

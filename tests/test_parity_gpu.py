@@ -42,6 +42,11 @@ def _gpu(cuda_device):
     (2, 2, 333, 333, 128, F16, False),
     (1, 1, 5, 1, 64, BF16, False),          # one key: O = V
     (3, 1, 384, 384, 64, F16, True),
+    # at most 128 query rows at d = 64: two heads per unit (head-pair mode)
+    (1, 3, 77, 77, 64, BF16, True),         # odd head count: the last unit has one head
+    (2, 2, 128, 128, 64, F16, False),
+    (1, 5, 2, 700, 64, BF16, False),        # two rows against a longer context
+    (2, 3, 100, 300, 64, F16, True),        # bottom-right causal mask, six heads
 ])
 def test_prefill_matches_oracle(shape):
     B, h, tq, tk, d, dt, causal = shape
