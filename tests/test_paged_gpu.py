@@ -203,6 +203,12 @@ TC_CASES = [
     (3, 4, 1, [1000, 7, 517], 64, BF16, 16, 0),
     (3, 4, 1, [300, 0, 50], 64, BF16, 16, 1),       # length 0, one partition: o = 0
     (4, 8, 1, [0, 2000, 64, 900], 64, F16, 8, 0),   # length 0 in a unit's first head
+    # pages of >= 64 rows at d = 64: two heads per unit, each with its own
+    # page lookups (pipelined one key tile ahead)
+    (3, 4, 1, [1000, 7, 517], 64, BF16, 64, 0),
+    (4, 8, 1, [0, 2000, 64, 900], 64, F16, 128, 0),
+    (3, 4, 1, [300, 0, 50], 64, BF16, 256, 1),      # length 0, one partition: o = 0
+    (2, 8, 2, [4000, 3000], 64, BF16, 64, 3),
 ]
 
 
