@@ -342,6 +342,13 @@ def run_ours(args):
     pre_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     step_ms = max_over_ranks(total_ms / K, world, dev)
+    # the K steps as 5 back-to-back repeats (>= 20 steps each at the default K):
+    # median and spread of the per-repeat step time
+    R = 5 if K >= 5 else 1
+    per = K // R
+    rep_ms = [ev[r * per][0].elapsed_time(ev[r * per + per - 1][2]) / per for r in range(R)]
+    repeats = {"n": R, "steps_each": per, "ms_per_step_median": statistics.median(rep_ms),
+               "spread_pct": 100.0 * (max(rep_ms) - min(rep_ms)) / statistics.median(rep_ms)}
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, the two calls, D2H of both outputs, every step
@@ -414,6 +421,12 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": 3 * K,
+        "repeats": repeats,
+        # device memory the library needs beyond the caller's inputs and
+        # outputs: the decode's split partials (stream-ordered, per call); the
+        # prefill needs none (the T x T scores never exist)
+        "extra_device_bytes": {"prefill": 0, "decode": _lib.workspace_bytes(
+            DECODE.B, DECODE.h, DECODE.T_q, DECODE.T_kv, DECODE.d, 0)},
         "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source")},
     }
     if world == 1 and not args.no_cpu_baseline:
