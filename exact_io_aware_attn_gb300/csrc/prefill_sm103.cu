@@ -85,10 +85,6 @@ struct Cfg {
   static constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  // of every 8 column pairs, how many take the polynomial exp2 (the rest
-  // use the special-function unit). Measured on GB300: the special-function
-  // unit keeps up at both widths, so every pair uses it.
-  static constexpr int POLY_PAIRS_OF_8 = 0;
   // d = 64 leaves TMEM room (S 2x128 + O 2x64 = 384 columns) for P in
   // columns of its own (2x64): S_X(j+1) can then be computed as soon as the
   // softmax has read S_X(j), while P_X(j) and PV_X(j) are still in flight,
@@ -120,28 +116,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
-}
-
-// 2^x on the FMA pipe for a pair of values: x = r + f with r = rint(x),
-// f in [-1/2, 1/2]; 2^f by a degree-3 polynomial with minimax relative
-// error 7.5e-5 on that interval (coefficients from a Remez exchange on the
-// relative error), and r added to the exponent field in the integer domain.
-// Packed fp32x2 arithmetic does two elements per instruction. x is clamped
-// at -125 (a result of 2^-125 stands in for 0: negligible against l >= 2^-8).
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x.x = fmaxf(x.x, -125.f);
-  x.y = fmaxf(x.y, -125.f);
-  const float2 t = __fadd2_rn(x, make_float2(12582912.f, 12582912.f));  // 1.5 * 2^23
-  const float2 r = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));  // rint(x), exact
-  const float2 f = __ffma2_rn(r, make_float2(-1.f, -1.f), x);             // x - r, exact
-  float2 p = __ffma2_rn(make_float2(0.0551716685f, 0.0551716685f), f,
-                        make_float2(0.242611125f, 0.242611125f));
-  p = __ffma2_rn(p, f, make_float2(0.693260968f, 0.693260968f));
-  p = __ffma2_rn(p, f, make_float2(0.999928057f, 0.999928057f));
-  // t carries r in its low mantissa bits; shifting them to the exponent
-  // field and adding scales p by 2^r
-  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
-                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -809,12 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; c += 2) {
           const float2 xx = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, nm2);
           float2 pp;
-          if (((c >> 1) & 7) < C::POLY_PAIRS_OF_8) {
-            pp = exp2_poly2(xx);
-          } else {
-            pp.x = ptx::ex2_approx(xx.x);
-            pp.y = ptx::ex2_approx(xx.y);
-          }
+          pp.x = ptx::ex2_approx(xx.x);
+          pp.y = ptx::ex2_approx(xx.y);
           rs2[(c >> 1) & 3] = __fadd2_rn(rs2[(c >> 1) & 3], pp);
           pk[c >> 1] = pack2<BF16>(pp.x, pp.y);
         }
