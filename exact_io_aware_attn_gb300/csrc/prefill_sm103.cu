@@ -332,10 +332,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == kWarpProducer) {
       // ------------------------------------------------------------ producer
-      if (lane == 0) {
-        ptx::prefetch_tensormap(&tmQ);
-        ptx::prefetch_tensormap(&tmK);
-        ptx::prefetch_tensormap(&tmV);
+      // One lane, except with a paged cache: there the whole warp runs the
+      // loop (its waits made warp-uniform) and lane i looks up and loads box
+      // i of each key tile, so a tile's table reads and copies run side by
+      // side instead of one after another.
+      if (PAGED || lane == 0) {
+        const bool lead = lane == 0;
+        auto uniform = [&](bool v) -> bool {
+          if constexpr (PAGED) return __all_sync(0xffffffffu, v) != 0;
+          return v;
+        };
+        if (lead) {
+          ptx::prefetch_tensormap(&tmQ);
+          ptx::prefetch_tensormap(&tmK);
+          ptx::prefetch_tensormap(&tmV);
+        }
         const uint64_t pol_kv = ptx::policy_evict_last();
         const uint64_t pol_q = ptx::policy_evict_first();
         uint32_t g = 0;   // ring fills issued
@@ -346,46 +357,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (u >= U) continue;
           const Unit w = unit_info<HP>(u, BH, n_pairs, T_q, T_kv, causal, h_q, h_kv, S, pkv.lens);
           if (w.n_all == 0) continue;  // a key partition the pair does not reach
-          ok = ptx::mbar_wait(q_empty, (nq & 1) ^ 1, status, status_word(kKernPrefill, kSiteProdQ));
+          ok = uniform(ptx::mbar_wait(q_empty, (nq & 1) ^ 1, status,
+                                      status_word(kKernPrefill, kSiteProdQ)));
           if (!ok) break;
-          ptx::mbar_arrive_expect_tx(q_full, C::TILE_BYTES * (w.rows_b > 0 ? 2 : 1));
+          if (lead) {
+            ptx::mbar_arrive_expect_tx(q_full, C::TILE_BYTES * (w.rows_b > 0 ? 2 : 1));
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            ptx::tma_load_3d(smem + C::OFF_Q + c * kSub, &tmQ, q_full, c * 64, w.q0, w.bh, pol_q);
-            if (w.rows_b > 0)
-              ptx::tma_load_3d(smem + C::OFF_Q + C::TILE_BYTES + c * kSub, &tmQ, q_full, c * 64,
-                               w.q0_b, w.bh_b, pol_q);
+            for (int c = 0; c < D / 64; ++c) {
+              ptx::tma_load_3d(smem + C::OFF_Q + c * kSub, &tmQ, q_full, c * 64, w.q0, w.bh, pol_q);
+              if (w.rows_b > 0)
+                ptx::tma_load_3d(smem + C::OFF_Q + C::TILE_BYTES + c * kSub, &tmQ, q_full, c * 64,
+                                 w.q0_b, w.bh_b, pol_q);
+            }
           }
           ++nq;
           if constexpr (!HP) {
             // one stream for both tiles: K_j, V_j
             for (int j = 0; ok && j < w.n_all; ++j) {
+              int pg = 0;  // paged: this lane's box of key tile j (shared by K_j and V_j)
 #pragma unroll
               for (int kind = 0; kind < 2; ++kind) {  // K_j, then V_j
                 const uint32_t slot = g % SL;
-                ok = ptx::mbar_wait(&slot_empty[slot], ((g / SL) & 1) ^ 1, status,
-                                    status_word(kKernPrefill, kSiteProdSlot));
+                ok = uniform(ptx::mbar_wait(&slot_empty[slot], ((g / SL) & 1) ^ 1, status,
+                                            status_word(kKernPrefill, kSiteProdSlot)));
                 if (!ok) break;
-                ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
+                if (lead) ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
                 uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
                 if constexpr (PAGED) {
-                  // the tile's 128 keys in boxes of min(page_size, 128) rows, each
-                  // from the page the table names (rows past the length: page 0,
-                  // masked later; a bad entry is reported, never dereferenced)
+                  // the tile's 128 keys in boxes of min(page_size, 128) rows,
+                  // box i from the page the table names, by lane i (rows past
+                  // the length: page 0, masked later; a bad entry is
+                  // reported, never dereferenced). The copies start after the
+                  // lead lane has announced the tile's bytes.
+                  __syncwarp();
                   const int rows = min(1 << pkv.page_shift, kBN);
                   const int b = w.bh / h_q;  // sequence of this virtual head
                   const int kvh = w.bh - b * h_q;
-                  for (int i = 0; i < kBN; i += rows) {
-                    const int key = (w.j0 + j) * kBN + i;
-                    int pg = 0;
-                    if (key < w.tkv) {
-                      pg = __ldg(pkv.table + static_cast<size_t>(b) * pkv.max_pages +
-                                 (key >> pkv.page_shift));
-                      if (static_cast<unsigned>(pg) >= static_cast<unsigned>(pkv.num_pages)) {
-                        atomicCAS(status, 0u,
-                                  status_word_code(1u /* ATTN_ERR_INVALID_ARG */, kKernPrefill,
-                                                   kSiteBadPage));
-                        pg = 0;
+                  const int i = lane * rows;
+                  const int key = (w.j0 + j) * kBN + i;
+                  if (i < kBN) {
+                    if (kind == 0) {
+                      pg = 0;
+                      if (key < w.tkv) {
+                        pg = __ldg(pkv.table + static_cast<size_t>(b) * pkv.max_pages +
+                                   (key >> pkv.page_shift));
+                        if (static_cast<unsigned>(pg) >= static_cast<unsigned>(pkv.num_pages)) {
+                          atomicCAS(status, 0u,
+                                    status_word_code(1u /* ATTN_ERR_INVALID_ARG */, kKernPrefill,
+                                                     kSiteBadPage));
+                          pg = 0;
+                        }
                       }
                     }
 #pragma unroll
@@ -436,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (!ok) {
+        if (!ok && lead) {
           // Error path: let the copies in flight land before the CTA (and its
           // shared memory) goes away. Only the last SLOTS fills and the last
           // Q load can still be outstanding.
