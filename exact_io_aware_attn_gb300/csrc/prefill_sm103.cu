@@ -1,26 +1,35 @@
-// prefill_sm103.cu -- exact attention forward for T_q > 1 on GB300 tensor cores.
+// prefill_sm103.cu -- exact attention forward for T_q > 1 on GB300 tensor cores
+// (also the grouped-query and paged decode of groups >= 4, as prefills of G
+// query rows per key/value head).
 //
-// A persistent CTA owns a sequence of work units; a unit is a pair of
-// 128-row query tiles (A and B) of one (batch, head) that share one stream of
-// 128-key K/V tiles. Roles (384 threads, three warpgroups):
+// A persistent CTA owns a sequence of work units. A unit is two 128-row
+// query tiles, A and B: rows [q0, q0+128) and [q0+128, q0+256) of one head
+// sharing one stream of 128-key K/V tiles (row pairs), or, for at most 128
+// query rows at d = 64, the rows of two heads with a K/V stream each (head
+// pairs). With S > 1 a unit covers one key partition and writes fp32
+// partials (o, m, l) for the merge kernel instead of O and lse. Roles (384
+// threads, three warpgroups):
 //
 //   warps 0-3     softmax of tile A; thread t owns query row t (TMEM lane t)
 //   warps 4-7     softmax of tile B
-//   warp 8        TMA producer: Q_A, Q_B once per unit, then K_j, V_j into a
-//                 ring of shared-memory slots (128-byte swizzle)
-//   warp 9        TMEM owner and MMA issuer (one thread)
-//   warps 10-11   no role; their warpgroup hands its registers to softmax
+//   warp 8        TMA producer: Q_A, Q_B once per unit, then K and V tiles into
+//                 a ring of shared-memory slots (128-byte swizzle); one lane,
+//                 or the whole warp with a paged cache (lane i gathers box i)
+//   warp 9        TMEM owner and MMA issuer (elected lane, warp-uniform loop);
+//                 at d = 64 it issues tile A's products and warp 10 tile B's
+//   warps 10-11   otherwise no role; their warpgroup hands its registers to
+//                 the softmax warpgroups
 //
 // Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A and O_B after
-// them (d columns each). S_X = Q_X K_j^T is one tcgen05.mma chain (M=128,
-// N=128) from shared memory; the softmax warps turn it into P_X =
-// 2^(scale*log2e*S_X - m) and store P_X as 16-bit back into the first 64
-// columns of S_X; O_X += P_X V_j then reads P from tensor memory and V from
-// shared memory. The issue order S_A(j), S_B(j), PV_A(j), S_A(j+1), PV_B(j),
-// S_B(j+1), ... keeps the tensor core busy on one tile while the other
-// tile's softmax runs (ping-pong), and the in-order execution of one
-// thread's tcgen05.mma makes every S_X(j+1) overwrite P_X(j) only after
-// PV_X(j) has read it.
+// them (d columns each); at d = 64 P_A and P_B have columns of their own
+// after O, at d = 128 P_X overwrites the first 64 columns of S_X. S_X = Q_X
+// K_j^T is a tcgen05.mma chain (M=128, N=128) from shared memory; the softmax
+// warps turn it into P_X = 2^(scale*log2e*S_X - m) as 16-bit values; O_X +=
+// P_X V_j reads P from tensor memory and V from shared memory. The tensor
+// core works on one tile while the other tile's softmax runs. At d = 128 one
+// thread issues both tiles in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1),
+// so S_X(j+1) overwrites P_X(j) only after PV_X(j) read it; at d = 64 each
+// tile's issuer starts S_X(j+1) as soon as its softmax has loaded S_X(j).
 //
 // Scores and probabilities never leave the chip; O is written to HBM once.
 // This is the tiled forward of "FlashAttention IO-aware tiling lab" ("Read
