@@ -12,9 +12,15 @@
 // partitions produces a partial output and a partial normaliser, combined
 // with the same rescaling by a second kernel):
 //
-//   decode_split_kernel    grid B*h*S: partition s of (b, h) streams its
-//                          keys once, keeps the online-softmax state
-//                          (m, l, o) in fp32 and writes it to the workspace.
+//   decode_split_1head_kernel  grid B*h*S: partition s of (b, h) streams
+//                          its keys once, keeps the online-softmax state
+//                          (m, l, o) in fp32 and writes it to the workspace
+//                          (8 resident CTAs per SM).
+//   decode_split_kernel<G = 2>  grouped-query heads in pairs: every cached
+//                          row is read once for both query heads (groups of
+//                          4 or more run on the tensor cores instead).
+//   decode_paged_split_kernel  the same loop with keys gathered through a
+//                          block table (paged cache, per-sequence lengths).
 //   decode_combine_kernel  one warp per (b, h): M = max m_s,
 //                          w_s = 2^(m_s - M), L = sum w_s l_s,
 //                          O = sum w_s o_s / L, lse = (M + log2 L) ln 2;
