@@ -1,6 +1,8 @@
 // attn_api.cu -- the C ABI of libattn (declared in include/attn.h): argument
-// validation, prefill/decode/backward dispatch, decode split choice,
-// stream-ordered workspace and the device status word. All compute happens
+// validation; dispatch of prefill, decode (CUDA cores, or the tensor cores
+// for grouped-query groups of 4 or more), paged decode, split-KV prefill and
+// backward; the split-count choices; stream-ordered workspace; the
+// host-buffer entry's copies; and the device status word. All compute happens
 // in the kernels of prefill_sm103.cu, decode_sm103.cu and backward_sm103.cu;
 // nothing here computes attention.
 #include <cuda_runtime.h>
