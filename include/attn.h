@@ -305,8 +305,10 @@ size_t attn_bwd_workspace_bytes(int B, int h, int T_q, int T_kv, int d);
  * page_size: a power of two, 1..65536. A length above
  * max_pages_per_seq * page_size is clamped to it; a length <= 0 gives
  * o = 0 and lse = -inf for that sequence. A table entry outside
- * [0, num_pages) is not dereferenced: its keys are skipped and the kernel
- * records ATTN_ERR_INVALID_ARG in the device status word (read it with
+ * [0, num_pages) is never dereferenced (the CUDA-core kernel skips those
+ * keys, the tensor-core path reads page 0 in their place, so that
+ * sequence's outputs are unspecified) and the kernel records
+ * ATTN_ERR_INVALID_ARG in the device status word (read it with
  * attn_get_device_error). Each sequence's keys are cut into num_splits
  * partitions (0 = the library's choice from max_pages_per_seq * page_size)
  * merged exactly as in attn_fwd's decode path. workspace: at least
