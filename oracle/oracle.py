@@ -38,13 +38,14 @@ Pages followed (cited by page title and section):
   oracle takes the plainest reading, the derivative of the forward above
   written out by the chain rule (attention_backward).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * Causal alignment when T_q != T_kv: bottom-right. Query row i may see key j
-  iff j <= i + (T_kv - T_q). For T_q == T_kv this is the pages' "position i
-  sees i keys" (1-based); for one query against a cache it sees every key.
+  iff j <= i + (T_kv - T_q). For T_q == T_kv this is the pages' definition
+  (row i, counted from 1, sees the first i keys); for one query against a
+  cache it sees every key.
 * lse is the natural log of sum_j exp(scale * q_i . k_j), in the units of
-  the scaled scores (the "per-row normalisation constant").
+  the scaled scores (the per-row normaliser the pages keep for the backward).
 * The scale is applied to the dot product (scores = k @ q / sqrt(d)); callers
   may pass any finite scale, default 1/sqrt(d).
 
