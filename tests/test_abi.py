@@ -396,3 +396,19 @@ def test_host_buffer_bytes(L):
     assert _lib.host_buffer_bytes(1, 4, 3, 256, 1024, 64) == 0   # h_q not a multiple of h_kv
     assert _lib.host_buffer_bytes(0, 4, 2, 256, 1024, 64) == 0
     assert _lib.host_buffer_bytes(1, 4, 2, 256, 1024, 96) == 0
+
+
+def test_host_binding_rejects_bad_tensors(L):
+    """attn_fwd_host's wrapper checks shapes and dtypes before any library
+    or CUDA call: 4-D contiguous CPU tensors of one 16-bit dtype."""
+    import torch
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        _lib.attn_fwd_host(q[0], q[0], q[0])                      # 3-D
+    with pytest.raises(ValueError):
+        _lib.attn_fwd_host(q, q.transpose(2, 3), q)                 # not contiguous
+    with pytest.raises(TypeError):
+        _lib.attn_fwd_host(q, q.to(torch.float16), q)               # mixed dtypes
+    with pytest.raises(ValueError):
+        _lib.attn_fwd_host(q, torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16),
+                           torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16))  # d differs
