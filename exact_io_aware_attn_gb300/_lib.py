@@ -8,6 +8,7 @@ an exception says so.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -135,21 +136,15 @@ def attn_fwd_gqa(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_s
     with h_q a multiple of h_kv. Returns (o like q, lse [B, h_q, T_q] fp32).
     The decode workspace comes from the library's stream-ordered allocation."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
-    if not (q.dtype == k.dtype == v.dtype):
-        raise TypeError("q, k and v must share one dtype")
-    B, h_q, T_q, d = q.shape
-    h_kv, T_kv = k.shape[1], k.shape[2]
-    if k.shape != (B, h_kv, T_kv, d) or v.shape != k.shape:
-        raise ValueError("k and v must be [B, h_kv, T_kv, d]")
+    B, h_q, h_kv, T_q, T_kv, d = _check_qkv(q, k, v)
+    _same_device(q, k=k, v=v)
     if scale is None:
         scale = d ** -0.5
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, h_q, T_q), dtype=torch.float32, device=q.device)
+    _check_outputs(q, out, lse, (B, h_q, T_q))
     with torch.cuda.device(q.device):
         st = fwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                          B, h_q, h_kv, T_q, T_kv, d, scale, causal, _dtype_code(q), num_splits,
@@ -163,6 +158,74 @@ def selftest_wait_timeout(limit_us, stream=None) -> int:
     """Enqueue the failure-detection self-test (a bounded wait that runs
     out after limit_us); returns the status of the enqueue."""
     return int(lib().attn_selftest_wait_timeout(int(limit_us), _stream_ptr(stream)))
+
+
+def _tensor(name, t, *, cuda=True, dim=None, shape=None, dtype=None):
+    """Checks one tensor argument before anything reaches the library: the
+    kind of memory (CUDA or CPU), rank, shape, dtype and contiguity. A wrong
+    kind of tensor or dtype raises TypeError, the rest ValueError. The
+    library reads raw addresses, so a tensor that is too small or strided
+    would otherwise be read or written out of bounds."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda is not cuda:
+        raise TypeError(f"{name} must be a {'CUDA' if cuda else 'CPU'} tensor")
+    if shape is not None:
+        if t.shape != shape:
+            raise ValueError(f"{name} must be shaped {tuple(shape)}, not {tuple(t.shape)}")
+    elif dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions, not {t.dim()}")
+    if dtype is not None and t.dtype is not dtype:
+        raise TypeError(f"{name} must be {dtype}, not {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _same_device(q, **tensors):
+    """Every CUDA tensor of one call lives on q's device (the library runs on
+    the current device, which the wrappers set to q's)."""
+    dev = q.get_device()
+    for name, t in tensors.items():
+        if t is not None and t.get_device() != dev:
+            raise ValueError(f"{name} is on {t.device} but q on {q.device}: one device per call")
+
+
+def _buffer(name, buf, device):
+    """(address, bytes) of an optional caller buffer: a contiguous CUDA
+    tensor on `device`, or (None, 0) when absent."""
+    if buf is None:
+        return None, 0
+    _tensor(name, buf)
+    if buf.device != device:
+        raise ValueError(f"{name} is on {buf.device} but must be on {device}")
+    return buf.data_ptr(), buf.numel() * buf.element_size()
+
+
+def _check_qkv(q, k, v, *, cuda=True):
+    """q [B, h_q, T_q, d]; k, v [B, h_kv, T_kv, d]; one 16-bit dtype.
+    Returns (B, h_q, h_kv, T_q, T_kv, d)."""
+    _tensor("q", q, cuda=cuda, dim=4)
+    _tensor("k", k, cuda=cuda, dim=4, dtype=q.dtype)
+    B, h_q, T_q, d = q.shape
+    Bk, h_kv, T_kv, dk = k.shape
+    if Bk != B or dk != d:
+        raise ValueError(f"k must be [B, h_kv, T_kv, d] with q's B = {B} and d = {d}, "
+                         f"not {tuple(k.shape)}")
+    _tensor("v", v, cuda=cuda, shape=k.shape, dtype=q.dtype)
+    _dtype_code(q)
+    return B, h_q, h_kv, T_q, T_kv, d
+
+
+def _check_outputs(q, out, lse, lse_shape, *, cuda=True):
+    """out like q (same shape and dtype), lse fp32 of lse_shape; both
+    contiguous, on q's device when they are CUDA tensors."""
+    import torch
+    _tensor("out", out, cuda=cuda, shape=q.shape, dtype=q.dtype)
+    _tensor("lse", lse, cuda=cuda, shape=lse_shape, dtype=torch.float32)
+    if cuda:
+        _same_device(q, out=out, lse=lse)
 
 
 def _stream_ptr(stream):
@@ -205,22 +268,20 @@ def attn_fwd_decode_noalloc(q, k, v, *, out, lse, scale=None, num_splits=0, stre
     race on it. q: [B, h, 1, d]; k, v: [B, h, T_kv, d]; out like q; lse
     [B, h, 1] fp32."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    B, h, T_q, d = q.shape
+    B, h, h_kv, T_q, T_kv, d = _check_qkv(q, k, v)
     if T_q != 1:
         raise ValueError("attn_fwd_decode_noalloc takes one query row per (b, h)")
-    T_kv = k.shape[2]
-    if k.shape != (B, h, T_kv, d) or v.shape != k.shape or out.shape != q.shape:
-        raise ValueError("shape mismatch")
-    if not (q.dtype == k.dtype == v.dtype == out.dtype) or lse.dtype != torch.float32:
-        raise TypeError("q, k, v, out share one 16-bit dtype; lse is fp32")
+    if h_kv != h:
+        raise ValueError("attn_fwd_decode_noalloc takes one key/value head per query head")
+    _same_device(q, k=k, v=v)
+    _check_outputs(q, out, lse, (B, h, 1))
     if scale is None:
         scale = d ** -0.5
-    st = fwd_decode_noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                lse.data_ptr(), B, h, T_kv, d, scale, _dtype_code(q), num_splits,
-                                _stream_ptr(stream))
+    # the library looks the scratch address up for the current device
+    with torch.cuda.device(q.device):
+        st = fwd_decode_noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), B, h, T_kv, d, scale, _dtype_code(q),
+                                    num_splits, _stream_ptr(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_decode_noalloc")
     return out, lse
@@ -246,19 +307,10 @@ def attn_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_split
     with torch if not given). Asynchronous on the current (or given) stream.
     """
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda:
-            raise TypeError(f"{name} must be a CUDA tensor")
-        if t.dim() != 4:
-            raise ValueError(f"{name} must be [B, h, T, d]")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-    if not (q.dtype == k.dtype == v.dtype):
-        raise TypeError("q, k and v must share one dtype")
-    B, h, T_q, d = q.shape
-    T_kv = k.shape[2]
-    if k.shape != (B, h, T_kv, d) or v.shape != (B, h, T_kv, d):
-        raise ValueError("k and v must be [B, h, T_kv, d] with q's B, h and d")
+    B, h, h_kv, T_q, T_kv, d = _check_qkv(q, k, v)
+    if h_kv != h:
+        raise ValueError("k and v must have q's number of heads (attn_fwd_gqa takes fewer)")
+    _same_device(q, k=k, v=v)
     dt = _dtype_code(q)
     if scale is None:
         scale = d ** -0.5
@@ -266,12 +318,9 @@ def attn_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_split
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, h, T_q), dtype=torch.float32, device=q.device)
-    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor like q")
-    if lse.shape != (B, h, T_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 [B, h, T_q] tensor")
-    sp = _stream_ptr(stream)
+    _check_outputs(q, out, lse, (B, h, T_q))
     with torch.cuda.device(q.device):
+        sp = _stream_ptr(stream)          # q's device's current stream when none is given
         if num_splits is None:
             st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                          B, h, T_q, T_kv, d, scale, causal, dt, sp)
@@ -279,8 +328,7 @@ def attn_fwd(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_split
             need = workspace_bytes(B, h, T_q, T_kv, d, num_splits)
             if workspace is None and need > 0:
                 workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-            wp = workspace.data_ptr() if workspace is not None else None
-            wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+            wp, wn = _buffer("workspace", workspace, q.device)
             st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                          B, h, T_q, T_kv, d, scale, causal, dt, sp, num_splits, wp, wn)
     if st != ATTN_OK:
@@ -315,29 +363,19 @@ def attn_bwd(q, k, v, o, lse, dout, *, scale=None, causal=False, dq=None, dk=Non
     forward with the same scale and causal flag. The workspace is taken
     stream-ordered by the library unless given. Asynchronous."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
-    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
-        raise TypeError("q, k, v, o and dout must share one dtype")
-    B, h_q, T_q, d = q.shape
-    h_kv, T_kv = k.shape[1], k.shape[2]
-    if k.shape != (B, h_kv, T_kv, d) or v.shape != k.shape:
-        raise ValueError("k and v must be [B, h_kv, T_kv, d]")
-    if o.shape != q.shape or dout.shape != q.shape:
-        raise ValueError("o and dout must be shaped like q")
-    if lse.shape != (B, h_q, T_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 [B, h_q, T_q] tensor")
+    B, h_q, h_kv, T_q, T_kv, d = _check_qkv(q, k, v)
+    _tensor("o", o, shape=q.shape, dtype=q.dtype)
+    _tensor("dout", dout, shape=q.shape, dtype=q.dtype)
+    _tensor("lse", lse, shape=(B, h_q, T_q), dtype=torch.float32)
     if scale is None:
         scale = d ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
-        if t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous tensor like its input")
-    wp = workspace.data_ptr() if workspace is not None else None
-    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _tensor(name, t, shape=like.shape, dtype=like.dtype)
+    _same_device(q, k=k, v=v, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv)
+    wp, wn = _buffer("workspace", workspace, q.device)
     with torch.cuda.device(q.device):
         st = bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, h_q, h_kv,
@@ -369,28 +407,31 @@ def attn_fwd_paged_decode(q, k_pages, v_pages, block_table, seq_lens, *, scale=N
     [B, max_pages]; seq_lens: int32 [B]; all contiguous CUDA tensors.
     Returns (o like q, lse [B, h_q] fp32)."""
     import torch
-    for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
-                    ("block_table", block_table), ("seq_lens", seq_lens)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    if k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
-        raise ValueError("k_pages and v_pages must be [num_pages, h_kv, page_size, d]")
-    if not (q.dtype == k_pages.dtype == v_pages.dtype):
-        raise TypeError("q and the page pools must share one dtype")
-    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
-        raise TypeError("block_table and seq_lens must be int32")
-    num_pages, h_kv, page_size, d = k_pages.shape
-    B, h_q = q.shape[0], q.shape[1]
-    if q.shape[-1] != d or q.numel() != B * h_q * d:
+    _tensor("q", q)
+    if q.dim() not in (3, 4) or (q.dim() == 4 and q.shape[2] != 1):
         raise ValueError("q must be [B, h_q, d] or [B, h_q, 1, d]")
-    if block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
-        raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
+    _tensor("k_pages", k_pages, dim=4, dtype=q.dtype)
+    num_pages, h_kv, page_size, d = k_pages.shape
+    _tensor("v_pages", v_pages, shape=k_pages.shape, dtype=q.dtype)
+    B, h_q = q.shape[0], q.shape[1]
+    if q.shape[-1] != d:
+        raise ValueError(f"q's last dimension must be the pages' d = {d}")
+    _tensor("block_table", block_table, dim=2, dtype=torch.int32)
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    _tensor("seq_lens", seq_lens, shape=(B,), dtype=torch.int32)
+    _dtype_code(q)
     if scale is None:
         scale = d ** -0.5
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, h_q), dtype=torch.float32, device=q.device) if lse is None else lse
-    wp = workspace.data_ptr() if workspace is not None else None
-    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _tensor("out", out, shape=q.shape, dtype=q.dtype)
+    _tensor("lse", lse, dtype=torch.float32)
+    if tuple(lse.shape) not in ((B, h_q), tuple(q.shape[:-1])):
+        raise ValueError("lse must be [B, h_q] (or [B, h_q, 1] beside a [B, h_q, 1, d] q)")
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, block_table=block_table, seq_lens=seq_lens,
+                 out=out, lse=lse)
+    wp, wn = _buffer("workspace", workspace, q.device)
     with torch.cuda.device(q.device):
         st = paged_decode_raw(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
                               block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
@@ -420,17 +461,14 @@ def attn_fwd_splitkv(q, k, v, *, scale=None, causal=False, out=None, lse=None, n
     (0: the library's choice) and merged exactly. q [B, h_q, T_q, d]; k, v
     [B, h_kv, T_kv, d]. Returns (o like q, lse [B, h_q, T_q] fp32)."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
-    B, h_q, T_q, d = q.shape
-    h_kv, T_kv = k.shape[1], k.shape[2]
+    B, h_q, h_kv, T_q, T_kv, d = _check_qkv(q, k, v)
+    _same_device(q, k=k, v=v)
     if scale is None:
         scale = d ** -0.5
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, h_q, T_q), dtype=torch.float32, device=q.device) if lse is None else lse
-    wp = workspace.data_ptr() if workspace is not None else None
-    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check_outputs(q, out, lse, (B, h_q, T_q))
+    wp, wn = _buffer("workspace", workspace, q.device)
     with torch.cuda.device(q.device):
         st = splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                          B, h_q, h_kv, T_q, T_kv, d, scale, causal, _dtype_code(q), num_splits,
@@ -464,15 +502,7 @@ def attn_fwd_host(q, k, v, *, scale=None, causal=False, out=None, lse=None, devi
     tensor of at least host_buffer_bytes(...) bytes) holds the device copies;
     without it they come from the stream-ordered allocator."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D CPU tensor")
-    if not (q.dtype == k.dtype == v.dtype):
-        raise TypeError("q, k and v must share one dtype")
-    B, h_q, T_q, d = q.shape
-    h_kv, T_kv = k.shape[1], k.shape[2]
-    if k.shape != (B, h_kv, T_kv, d) or v.shape != k.shape:
-        raise ValueError("k and v must be [B, h_kv, T_kv, d] with q's B and d")
+    B, h_q, h_kv, T_q, T_kv, d = _check_qkv(q, k, v, cuda=False)
     dt = _dtype_code(q)
     if scale is None:
         scale = d ** -0.5
@@ -480,19 +510,17 @@ def attn_fwd_host(q, k, v, *, scale=None, causal=False, out=None, lse=None, devi
         out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     if lse is None:
         lse = torch.empty((B, h_q, T_q), dtype=torch.float32).pin_memory()
-    if out.is_cuda or out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous CPU tensor like q")
-    if lse.is_cuda or lse.shape != (B, h_q, T_q) or lse.dtype != torch.float32 or \
-            not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 CPU [B, h_q, T_q] tensor")
-    bp, bn = None, 0
+    _check_outputs(q, out, lse, (B, h_q, T_q), cuda=False)
+    bp, bn, where = None, 0, contextlib.nullcontext()
     if device_buffer is not None:
-        if not device_buffer.is_cuda:
-            raise ValueError("device_buffer must be a CUDA tensor")
+        _tensor("device_buffer", device_buffer)
         bp, bn = device_buffer.data_ptr(), device_buffer.numel() * device_buffer.element_size()
-    sp = _stream_ptr(stream)
-    st = fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                      B, h_q, h_kv, T_q, T_kv, d, scale, causal, dt, bp, bn, sp)
+        # the library works on the current device: make it the buffer's
+        where = torch.cuda.device(device_buffer.device)
+    with where:
+        st = fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, h_q, h_kv, T_q, T_kv, d, scale, causal, dt, bp, bn,
+                          _stream_ptr(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_host")
     if synchronize:

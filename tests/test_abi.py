@@ -412,3 +412,70 @@ def test_host_binding_rejects_bad_tensors(L):
     with pytest.raises(ValueError):
         _lib.attn_fwd_host(q, torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16),
                            torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16))  # d differs
+
+
+def test_device_wrappers_reject_host_tensors(L):
+    """Every wrapper that takes device tensors refuses CPU tensors with a
+    TypeError before any library call (a host address handed to a kernel
+    would fault)."""
+    import torch
+    x = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 8, dtype=torch.float32)
+    x1 = torch.zeros(1, 2, 1, 64, dtype=torch.bfloat16)
+    pages = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16)
+    table = torch.zeros(1, 4, dtype=torch.int32)
+    lens = torch.ones(1, dtype=torch.int32)
+    calls = [
+        lambda: _lib.attn_fwd(x, x, x),
+        lambda: _lib.attn_fwd_gqa(x, x, x),
+        lambda: _lib.attn_fwd_splitkv(x, x, x),
+        lambda: _lib.attn_bwd(x, x, x, x, lse, x),
+        lambda: _lib.attn_fwd_decode_noalloc(x1, x, x, out=x1, lse=lse[:, :, :1]),
+        lambda: _lib.attn_fwd_paged_decode(x1, pages, pages, table, lens),
+    ]
+    for call in calls:
+        with pytest.raises(TypeError):
+            call()
+
+
+def test_host_binding_checks_outputs_and_buffer(L):
+    """The shared checks on out and lse (shape, dtype, contiguity, kind of
+    memory) and on the device buffer, through attn_fwd_host: all fail before
+    any library call."""
+    import torch
+    q = torch.zeros(1, 4, 8, 64, dtype=torch.float16)
+    kv = torch.zeros(1, 2, 16, 64, dtype=torch.float16)      # grouped-query: 2 key/value heads
+    lse = torch.zeros(1, 4, 8, dtype=torch.float32)
+    bad = [
+        (dict(out=torch.zeros(1, 4, 8, 32, dtype=torch.float16), lse=lse), ValueError),  # shape
+        (dict(out=torch.zeros(1, 4, 8, 64, dtype=torch.bfloat16), lse=lse), TypeError),  # dtype
+        (dict(out=torch.zeros(1, 4, 64, 8, dtype=torch.float16).transpose(2, 3), lse=lse),
+         ValueError),
+        (dict(out=q.clone(), lse=torch.zeros(1, 4, 7)), ValueError),              # lse rows
+        (dict(out=q.clone(), lse=torch.zeros(1, 4, 8, dtype=torch.float64)), TypeError),
+        (dict(out=q.clone(), lse=torch.zeros(1, 8, 4).transpose(1, 2)), ValueError),
+        (dict(out=q.clone(), lse=lse, device_buffer=torch.zeros(1024, dtype=torch.uint8)),
+         TypeError),                                                             # not on a GPU
+        (dict(out=q.clone(), lse=lse, device_buffer=b"\0" * 1024), TypeError),   # not a tensor
+    ]
+    for kwargs, exc in bad:
+        with pytest.raises(exc):
+            _lib.attn_fwd_host(q, kv, kv, **kwargs)
+    with pytest.raises(ValueError):                                              # v unlike k
+        _lib.attn_fwd_host(q, kv, torch.zeros(1, 2, 15, 64, dtype=torch.float16), out=q, lse=lse)
+    with pytest.raises(TypeError):                                               # fp32 inputs
+        _lib.attn_fwd_host(q.float(), kv.float(), kv.float(), out=q.float(), lse=lse)
+    with pytest.raises(TypeError):
+        _lib.attn_fwd_host([q], kv, kv, out=q, lse=lse)
+
+
+def test_shared_checks_accept_valid_shapes():
+    """The checks pass the layouts the wrappers document: grouped-query k/v,
+    and (for the paged decode) q as [B, h_q, d] or [B, h_q, 1, d]."""
+    import torch
+    q = torch.zeros(2, 8, 5, 128, dtype=torch.bfloat16)
+    kv = torch.zeros(2, 2, 9, 128, dtype=torch.bfloat16)
+    assert _lib._check_qkv(q, kv, kv, cuda=False) == (2, 8, 2, 5, 9, 128)
+    _lib._check_outputs(q, torch.empty_like(q), torch.zeros(2, 8, 5), (2, 8, 5), cuda=False)
+    empty = torch.zeros(0, 8, 5, 128, dtype=torch.bfloat16)
+    assert _lib._check_qkv(empty, kv[:0], kv[:0], cuda=False)[0] == 0
