@@ -479,3 +479,73 @@ def test_shared_checks_accept_valid_shapes():
     _lib._check_outputs(q, torch.empty_like(q), torch.zeros(2, 8, 5), (2, 8, 5), cuda=False)
     empty = torch.zeros(0, 8, 5, 128, dtype=torch.bfloat16)
     assert _lib._check_qkv(empty, kv[:0], kv[:0], cuda=False)[0] == 0
+
+
+def test_fast_checks_accept_exactly_the_valid_calls():
+    """_check_qkv and _check_outputs try the valid case in one expression
+    and fall back to per-argument checks that raise. Over random argument
+    sets (ranks, dtypes, shapes, strides, a tensor subclass), each accepts
+    exactly the sets an independent statement of the rules accepts, and
+    returns the sizes that statement gives."""
+    import random
+
+    import torch
+    rng = random.Random(5)
+    dtypes = [torch.bfloat16, torch.float16, torch.float32]
+
+    def rand_tensor(shape, dtype):
+        t = torch.zeros(shape, dtype=dtype)
+        r = rng.random()
+        if r < 0.1 and t.dim() >= 2 and t.shape[-1] > 1 and t.shape[-2] > 1:
+            t = t.transpose(-1, -2)                          # strided view
+        elif r < 0.15:
+            t = torch.nn.Parameter(t, requires_grad=False)   # a Tensor subclass
+        return t
+
+    def shape4():
+        return [rng.choice([1, 2]), rng.choice([1, 2, 4]), rng.choice([1, 3, 5]),
+                rng.choice([64, 128])]
+
+    accepted = rejected = 0
+    for _ in range(3000):
+        qs = shape4()
+        ks = [qs[0], rng.choice([1, 2]), rng.choice([1, 7]), qs[3]]
+        vs = list(ks)
+        bad = rng.random()
+        if bad < 0.1:
+            ks[0] += 1
+        elif bad < 0.2:
+            vs[2] += 1
+        elif bad < 0.25:
+            qs = qs[:3]
+        dq = rng.choice(dtypes) if rng.random() < 0.3 else torch.bfloat16
+        dk = rng.choice(dtypes) if rng.random() < 0.1 else dq
+        q, k, v = rand_tensor(qs, dq), rand_tensor(ks, dk), rand_tensor(vs, dq)
+        ok = (q.dim() == 4 and k.dim() == 4 and q.dtype in (torch.bfloat16, torch.float16)
+              and k.dtype == q.dtype and v.dtype == q.dtype and k.shape[0] == q.shape[0]
+              and k.shape[3] == q.shape[3] and v.shape == k.shape
+              and all(t.is_contiguous() for t in (q, k, v)))
+        try:
+            got = _lib._check_qkv(q, k, v, cuda=False)
+        except (TypeError, ValueError):
+            got = None
+        assert (got is not None) == ok, (q.shape, q.dtype, k.shape, k.dtype, v.shape)
+        if ok:
+            assert got == (q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3])
+            out = rand_tensor(list(q.shape) if rng.random() < 0.8 else [1, 1, 1, 1],
+                              q.dtype if rng.random() < 0.9 else torch.float32)
+            lse_shape = list(q.shape[:3]) if rng.random() < 0.8 else [q.shape[0], q.shape[1]]
+            lse = rand_tensor(lse_shape, torch.float32 if rng.random() < 0.9 else torch.float64)
+            ok_out = (out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous()
+                      and tuple(lse.shape) == tuple(q.shape[:3]) and lse.dtype == torch.float32
+                      and lse.is_contiguous())
+            try:
+                _lib._check_outputs(q, out, lse, tuple(q.shape[:3]), cuda=False)
+                fine = True
+            except (TypeError, ValueError):
+                fine = False
+            assert fine == ok_out, (out.shape, out.dtype, lse.shape, lse.dtype)
+            accepted += 1
+        else:
+            rejected += 1
+    assert accepted > 500 and rejected > 500
