@@ -131,10 +131,12 @@ def fwd_gqa_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h_q, h_kv, T_q, T_kv, d,
 
 
 def attn_fwd_gqa(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_splits=0,
-                 stream=None):
+                 workspace=None, stream=None):
     """Grouped-query attention: q [B, h_q, T_q, d]; k, v [B, h_kv, T_kv, d]
     with h_q a multiple of h_kv. Returns (o like q, lse [B, h_q, T_q] fp32).
-    The decode workspace comes from the library's stream-ordered allocation."""
+    The decode workspace is `workspace` (a CUDA tensor of at least
+    gqa_workspace_bytes(...) bytes) or, when None, the library's
+    stream-ordered allocation."""
     import torch
     B, h_q, h_kv, T_q, T_kv, d = _check_qkv(q, k, v)
     _same_device(q, k=k, v=v)
@@ -145,10 +147,11 @@ def attn_fwd_gqa(q, k, v, *, scale=None, causal=False, out=None, lse=None, num_s
     if lse is None:
         lse = torch.empty((B, h_q, T_q), dtype=torch.float32, device=q.device)
     _check_outputs(q, out, lse, (B, h_q, T_q))
+    wp, wn = _buffer("workspace", workspace, q.device)
     with torch.cuda.device(q.device):
         st = fwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                          B, h_q, h_kv, T_q, T_kv, d, scale, causal, _dtype_code(q), num_splits,
-                         None, 0, _stream_ptr(stream))
+                         wp, wn, _stream_ptr(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_gqa")
     return out, lse
