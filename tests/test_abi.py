@@ -549,3 +549,27 @@ def test_fast_checks_accept_exactly_the_valid_calls():
         else:
             rejected += 1
     assert accepted > 500 and rejected > 500
+
+
+def test_splitkv_workspace_bytes(L):
+    """Split-KV prefill sizing: B*h*T_q*S*(d+4)*4 bytes for S partitions, 0
+    for one partition or invalid sizes. The library's own choice (S = 0) keeps
+    problems whose units fill half the SMs unsplit, and otherwise takes 2..64
+    partitions of at least two 128-key tiles each."""
+    assert _lib.splitkv_workspace_bytes(1, 8, 256, 16384, 128, 7) == 8 * 256 * 7 * 132 * 4
+    assert _lib.splitkv_workspace_bytes(2, 3, 100, 300, 64, 4) == 6 * 100 * 4 * 68 * 4
+    assert _lib.splitkv_workspace_bytes(1, 8, 256, 16384, 128, 1) == 0
+    assert _lib.splitkv_workspace_bytes(1, 8, 256, 16384, 128, 65) == 0     # above 64
+    assert _lib.splitkv_workspace_bytes(1, 8, 1, 16384, 128, 4) == 0        # one row: decode
+    assert _lib.splitkv_workspace_bytes(1, 8, 256, 16384, 96, 4) == 0       # unsupported d
+    assert _lib.splitkv_workspace_bytes(8, 12, 1024, 1024, 64, 0) == 0      # fills the device
+    for (B, h, T_q, T_kv, d) in ((1, 8, 256, 16384, 128), (1, 1, 300, 8192, 64),
+                                 (1, 2, 4096, 4096, 128), (2, 1, 200, 200, 64)):
+        nbytes = _lib.splitkv_workspace_bytes(B, h, T_q, T_kv, d, 0)
+        per_split = B * h * T_q * (d + 4) * 4
+        assert nbytes % per_split == 0
+        S = nbytes // per_split
+        n_kv = -(-T_kv // 128)
+        assert S == 0 or 2 <= S <= min(64, n_kv // 2), (B, h, T_q, T_kv, d, S)
+    # a long context behind a few query rows is split
+    assert _lib.splitkv_workspace_bytes(1, 8, 256, 16384, 128, 0) > 0
