@@ -115,3 +115,24 @@ def test_coarser_rounding_breaks_the_gate(dtype):
         o = rounding_model(q, k, v, True, oracle_scale(0.125), dtype, p_bits=bits - 2)
         worst = max(worst, gate_ratio(o, ref, dtype))
     assert worst > 1.0, f"4x coarser rounding of P stays at {worst:.2f} of the gate"
+
+
+@pytest.mark.parametrize("dtype,causal,pct", [(BF16, True, 3), (F16, True, 1), (BF16, False, 5),
+                                               (F16, False, 1)])
+def test_backward_gate_has_room_and_catches_a_small_dk_error(dtype, causal, pct):
+    """The gradients' gate (parity_helpers.compare_grads): the oracle's own
+    gradients rounded once to the 16-bit type pass with margin (about a
+    quarter of the gate or less), and dK off by a few percent fails. The
+    smallest caught error is 2% (bf16, causal), 3% (bf16, no mask) and 0.5%
+    (fp16): dK is a cancelling sum (its rows of dS sum to zero), so bf16's
+    gate leaves it more room."""
+    from exact_io_aware_attn_gb300.inputs import make_dout
+    from parity_helpers import compare_grads, oracle_bwd
+    q, k, v = make_qkv(1, 2, 200, 200, 64, dtype, 1.0, seed=21)
+    do = make_dout(1, 2, 200, 64, dtype, seed=21)
+    ref = oracle_bwd(q, k, v, do, causal)
+    rounded = [torch.from_numpy(g).to(TORCH_DT[dtype]).double().numpy() for g in ref[0]]
+    assert compare_grads(rounded, ref, dtype, "oracle rounded") <= 0.5
+    planted = [rounded[0], rounded[1] * (1 + pct / 100), rounded[2]]
+    with pytest.raises(AssertionError, match="dk"):
+        compare_grads(planted, ref, dtype, f"dK off by {pct}%")
