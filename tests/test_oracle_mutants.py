@@ -29,7 +29,7 @@ def _with(**over):
 
 
 def _std_factory(mask_fn=None, lse_fn=None, transpose_k=False, normalise=True,
-                 default_scale=lambda d: 1.0 / math.sqrt(d)):
+                 default_scale=lambda d: 1.0 / math.sqrt(d), rows_relative=False):
     def std(q, k, v, scale=None, causal=False, rows=None):
         q = np.asarray(q, dtype=np.float64)
         k = np.asarray(k, dtype=np.float64)
@@ -45,8 +45,11 @@ def _std_factory(mask_fn=None, lse_fn=None, transpose_k=False, normalise=True,
             kk = k[idx]
             s = scale * (q[idx][rws] @ (kk if transpose_k else kk.T))
             if causal:
+                # a selected row's causal position: its absolute index (or,
+                # planted, its position among the selected rows)
+                pos = np.arange(len(rws)) if rows_relative else rws
                 vis = (mask_fn or (lambda i, j, off: j <= i + off))(
-                    rws[:, None], np.arange(t_kv)[None, :], t_kv - t_q)
+                    pos[:, None], np.arange(t_kv)[None, :], t_kv - t_q)
                 s = np.where(vis, s, -np.inf)
             m = s.max(axis=1, keepdims=True)
             p = np.exp(s - m)
@@ -195,6 +198,7 @@ MUTANTS = {
     "backward_dv_unnormalised_p": _with(attention_backward=_bwd_factory(dv_unnormalised=True)),
     "backward_causal_excludes_diagonal": _with(attention_backward=_bwd_factory(causal_off=-1)),
     "gqa_backward_overwrites": _with(gqa_attention_backward=_gqa_bwd_overwrites),
+    "rows_relative_causal_positions": _with(standard_attention=_std_factory(rows_relative=True)),
     "paged_off_by_one_page": _with(paged_decode_attention=_paged_factory(page_off=1)),
     "paged_ignores_length": _with(paged_decode_attention=_paged_factory(ignore_len=True)),
     "paged_modulo_head_mapping": _with(paged_decode_attention=_paged_factory(head_modulo=True)),
