@@ -22,8 +22,11 @@ from ._lib import (  # noqa: F401
     decode_num_splits,
     fwd_raw,
     get_device_error,
+    gqa_workspace_bytes,
     host_buffer_bytes,
     last_kernel_name,
+    paged_workspace_bytes,
+    splitkv_workspace_bytes,
     status_string,
     workspace_bytes,
 )
