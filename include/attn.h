@@ -221,11 +221,12 @@ const char* attn_status_string(int status);
 int attn_abi_version(void);
 
 /*
- * attn_last_kernel_name -- static name of the kernel family the last
- * successful attn_fwd/attn_fwd_ex/attn_fwd_gqa/attn_bwd call on this host
- * thread enqueued ("prefill_tcgen05_d64_bf16",
+ * attn_last_kernel_name -- static name of the kernel family that the last
+ * successful call on this host thread enqueued ("prefill_tcgen05_d64_bf16",
  * "decode_split_d64_bf16+decode_combine", ... or "none" for an empty call),
- * so a benchmark can record which kernel ran.
+ * so a benchmark can record which kernel ran. Set by attn_fwd, attn_fwd_ex,
+ * attn_fwd_gqa, attn_fwd_splitkv, attn_fwd_paged_decode, attn_fwd_host,
+ * attn_bwd and attn_bwd_gqa; attn_fwd_decode_noalloc leaves it unchanged.
  */
 const char* attn_last_kernel_name(void);
 
