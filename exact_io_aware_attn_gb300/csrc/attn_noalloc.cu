@@ -18,7 +18,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "attn.h"
 #include "attn_internal.h"
@@ -30,21 +29,15 @@ constexpr size_t kScratchFloats = ATTN_NOALLOC_SCRATCH_BYTES / sizeof(float);
 // The library's own decode scratch: [B*h][S][d+4] fp32 partials.
 static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
 
-// Device address of g_decode_scratch for the current device, looked up once
-// per device. In host code the symbol names a host-side stand-in, not device
-// memory, so the kernels must receive this address instead.
+// Device address of g_decode_scratch on the current device. In host code the
+// symbol names a host-side stand-in, not device memory, so the kernels must
+// receive this address instead. It is looked up on every call (the lookup
+// enqueues nothing): an address kept from an earlier call would go stale if
+// the caller reset the device, which reloads the module elsewhere.
 float* scratch_ptr() {
-  static std::mutex mu;
-  static float* ptrs[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> g(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    ptrs[dev] = static_cast<float*>(p);
-  }
-  return ptrs[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+  return static_cast<float*>(p);
 }
 
 }  // namespace

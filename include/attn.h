@@ -379,8 +379,11 @@ size_t attn_splitkv_workspace_bytes(int B, int h_q, int T_q, int T_kv, int d, in
  * the library, ATTN_NOALLOC_SCRATCH_BYTES on every device that loads it,
  * held until the library is unloaded. A shape whose partials do not fit
  * returns ATTN_ERR_WORKSPACE before anything is enqueued (fewer splits may
- * fit). The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * fit). Every call looks up the array's device address on the current
+ * device (cudaGetSymbolAddress, which enqueues nothing, so a device reset
+ * between calls is safe); the first call on a device may also load the
+ * library's device code there, so make that first call before any stream
+ * capture.
  * All calls on a device share the array: calls whose kernels overlap on the
  * GPU (e.g. on two streams without ordering) race and give wrong results.
  * The array keeps the last call's partials; nothing in it needs clearing.

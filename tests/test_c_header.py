@@ -136,5 +136,9 @@ def test_header_is_plain_c_and_links(libpath, tmp_path):
            libpath, f"-Wl,-rpath,{libdir}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
-    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    # no GPU visible: every call here must return before touching CUDA, so a
+    # regression that moved a check after a launch fails with ATTN_ERR_CUDA
+    # instead of launching kernels on the fake addresses
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120, env=env)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
