@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     attn_fwd_decode_noalloc,
     attn_fwd_gqa,
     attn_fwd_host,
+    attn_fwd_naive,
     attn_fwd_paged_decode,
     attn_fwd_splitkv,
     decode_num_splits,
@@ -25,6 +26,7 @@ from ._lib import (  # noqa: F401
     gqa_workspace_bytes,
     host_buffer_bytes,
     last_kernel_name,
+    naive_workspace_bytes,
     paged_workspace_bytes,
     splitkv_workspace_bytes,
     status_string,

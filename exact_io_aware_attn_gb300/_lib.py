@@ -56,6 +56,8 @@ SIGNATURES = {
     "attn_fwd_host": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ,
                            _VP]),
     "attn_host_buffer_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_fwd_naive": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ, _VP]),
+    "attn_naive_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
 }
 
 # Bytes of the library-owned decode scratch behind attn_fwd_decode_noalloc.
@@ -497,6 +499,46 @@ def attn_fwd_splitkv(q, k, v, *, scale=None, causal=False, out=None, lse=None, n
                          wp, wn, _stream_ptr(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def naive_workspace_bytes(B, h, T_q, T_kv) -> int:
+    return int(lib().attn_naive_workspace_bytes(B, h, T_q, T_kv))
+
+
+def naive_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_q, T_kv, d, scale, causal, dtype,
+              workspace_ptr=None, workspace_nbytes=0, stream_ptr=None) -> int:
+    """Direct call of attn_fwd_naive; returns the status code."""
+    return int(lib().attn_fwd_naive(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, T_q, T_kv, d,
+                                    float(scale), int(causal), int(dtype), workspace_ptr,
+                                    int(workspace_nbytes), stream_ptr))
+
+
+def attn_fwd_naive(q, k, v, *, scale=None, causal=False, out=None, lse=None, workspace=None,
+                   stream=None):
+    """The materialising forward (S and P written to `workspace` as 16-bit
+    [B, h, T_q, T_kv] matrices, then O = P V): the comparison baseline for
+    the IO-aware kernels. q [B, h, T_q, d]; k, v [B, h, T_kv, d]. Returns (o
+    like q, lse [B, h, T_q] fp32). `workspace`: a CUDA uint8 tensor of at
+    least naive_workspace_bytes(...) bytes, else the stream-ordered
+    allocator supplies it."""
+    import torch
+    B, h, h_kv, T_q, T_kv, d = _check_qkv(q, k, v)
+    if h_kv != h:
+        raise ValueError("attn_fwd_naive takes one key/value head per query head")
+    _same_device(q, k=k, v=v)
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, h, T_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_outputs(q, out, lse, (B, h, T_q))
+    wp, wn = _buffer("workspace", workspace, q.device)
+    with torch.cuda.device(q.device):
+        st = naive_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, h, T_q, T_kv, d, scale, causal, _dtype_code(q), wp, wn,
+                       _stream_ptr(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_naive")
     return out, lse
 
 

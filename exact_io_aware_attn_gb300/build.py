@@ -26,7 +26,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 
 SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "backward_sm103.cu",
-           "attn_noalloc.cu", "tma_host.cu"]
+           "attn_noalloc.cu", "tma_host.cu", "naive_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

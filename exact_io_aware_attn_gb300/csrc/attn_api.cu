@@ -620,6 +620,47 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
   return st;
 }
 
+attn_status_t attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int h, int T_q, int T_kv, int d, float scale, int causal,
+                             int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  bool empty = false;
+  attn_status_t st = validate(q, k, v, o, lse, B, h, T_q, T_kv, d, scale, causal, dtype, &empty);
+  if (st != ATTN_OK) return st;
+  if (empty) {
+    t_last_kernel = "none";
+    return ATTN_OK;
+  }
+  const long long BH = static_cast<long long>(B) * h;
+  if (BH > 65535) return ATTN_ERR_UNSUPPORTED;  // one grid slice per head
+  const size_t need = attn::naive_workspace_bytes(BH, T_q, T_kv);
+  const bool own = workspace == nullptr && workspace_bytes == 0;
+  if (!own) {
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ATTN_ERR_WORKSPACE;
+    const size_t qo = static_cast<size_t>(BH) * T_q * d * 2;
+    const size_t kv = static_cast<size_t>(BH) * T_kv * d * 2;
+    if (overlaps(workspace, need, q, qo) || overlaps(workspace, need, k, kv) ||
+        overlaps(workspace, need, v, kv) || overlaps(workspace, need, o, qo) ||
+        overlaps(workspace, need, lse, static_cast<size_t>(BH) * T_q * 4))
+      return ATTN_ERR_WORKSPACE;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  if (own && cudaMallocAsync(&ws, need, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn::FwdProblem p{q, k, v, o, lse, B, h, T_q, T_kv, d, scale, causal,
+                     dtype == ATTN_BF16 ? 1 : 0, nullptr, h};
+  const char* name = "none";
+  const cudaError_t e = attn::launch_naive(p, ws, s, &name);
+  if (own) cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  t_last_kernel = name;
+  return ATTN_OK;
+}
+
+size_t attn_naive_workspace_bytes(int B, int h, int T_q, int T_kv) {
+  if (B < 0 || h < 0 || T_q < 0 || T_kv < 0) return 0;
+  return attn::naive_workspace_bytes(static_cast<long long>(B) * h, T_q, T_kv);
+}
+
 size_t attn_host_buffer_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int d) {
   size_t off[5];
   return host_region(B, h_q, h_kv, T_q, T_kv, d, off);

@@ -115,6 +115,14 @@ inline bool head_pair_mode(int d, int T_q, long long BH) { return d == 64 && T_q
 // Split kernel occupancy (CTAs per SM) for the split-count heuristic.
 int decode_split_ctas_per_sm(int d, int heads_per_cta);
 
+// The materialising baseline (naive_sm103.cu): S = scale * Q K^T and
+// P = softmax(S), both 16-bit [B*h][T_q][T_kv], written to `workspace`
+// (S first, then P), then O = P V; lse from the softmax pass.
+cudaError_t launch_naive(const FwdProblem& p, void* workspace, cudaStream_t stream, const char** name);
+inline size_t naive_workspace_bytes(long long BH, int T_q, int T_kv) {
+  return 2 * static_cast<size_t>(BH) * static_cast<size_t>(T_q) * static_cast<size_t>(T_kv) * 2;
+}
+
 namespace detail {
 // Argument checks shared by every entry point (attn_api.cu); *empty is set
 // when the output has no elements.

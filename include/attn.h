@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 typedef enum {
   ATTN_OK = 0,
@@ -95,7 +95,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
 /*
  * attn_fwd_ex -- attn_fwd with caller-chosen decode split count and
- * caller-owned workspace.
+ * caller-owned workspace. The split count is the number of key partitions
+ * whose partial (max, sum, output) are merged exactly ("IO-Aware
+ * Attention: Tiling the Score Matrix Without Materializing It", section
+ * "Parallelism and the cost of the split").
  *   num_splits  key partitions per (b, h) for the decode path: 0 = the
  *               library's choice by shape, else 1..1024 (a partition that
  *               gets no key contributes weight 0). Ignored for T_q > 1.
@@ -142,7 +145,8 @@ size_t attn_gqa_workspace_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int
  * shape (0 for the prefill path). num_splits as in attn_fwd_ex (0 = the
  * library's choice). Returns 0 for invalid sizes. The decode workspace holds
  * one partial (running max, running sum, unnormalised output of d floats)
- * per (b, h, split): B*h*S*(d+4)*4 bytes.
+ * per (b, h, split): B*h*S*(d+4)*4 bytes -- the per-partition state of
+ * "IO-Aware Attention ...", section "Parallelism and the cost of the split".
  */
 size_t attn_workspace_bytes(int B, int h, int T_q, int T_kv, int d, int num_splits);
 
@@ -226,7 +230,8 @@ int attn_abi_version(void);
  * "decode_split_d64_bf16+decode_combine", ... or "none" for an empty call),
  * so a benchmark can record which kernel ran. Set by attn_fwd, attn_fwd_ex,
  * attn_fwd_gqa, attn_fwd_splitkv, attn_fwd_paged_decode, attn_fwd_host,
- * attn_bwd and attn_bwd_gqa; attn_fwd_decode_noalloc leaves it unchanged.
+ * attn_fwd_naive, attn_bwd and attn_bwd_gqa; attn_fwd_decode_noalloc leaves
+ * it unchanged.
  */
 const char* attn_last_kernel_name(void);
 
@@ -362,6 +367,37 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
 /* attn_splitkv_workspace_bytes -- workspace attn_fwd_splitkv needs (0 for
  * invalid sizes or one partition). */
 size_t attn_splitkv_workspace_bytes(int B, int h_q, int T_q, int T_kv, int d, int num_splits);
+
+/*
+ * attn_fwd_naive -- the materialising forward, for comparison with the
+ * IO-aware kernels: the standard attention of "Attention and Its
+ * Computational Cost", section "The cost of writing down the scores" (one
+ * T_q x T_kv score tensor per head, then a softmax, then P V) and of "E8.1
+ * IO-aware attention" Part 2 (standard_attention). Three kernels write the
+ * whole score matrix S = scale * Q K^T (masked entries -inf) and the whole
+ * probability matrix P = softmax(S) to `workspace` as 16-bit
+ * [B][h][T_q][T_kv] matrices, then form O = P V; lse comes from the softmax
+ * pass. S and P are rounded to the 16-bit dtype (as a 16-bit framework
+ * stores them), so results differ from attn_fwd by that rounding.
+ * Arguments as attn_fwd (plain heads, h_kv == h); B*h <= 65535.
+ *   workspace  device memory of at least attn_naive_workspace_bytes(B, h,
+ *              T_q, T_kv) bytes (2 x B*h*T_q*T_kv x 2 bytes: S then P),
+ *              16-byte aligned, not overlapping any argument; NULL with
+ *              workspace_bytes 0: taken from and returned to the
+ *              stream-ordered allocator.
+ * Returns ATTN_ERR_WORKSPACE for a missing, short, misaligned or
+ * overlapping workspace, ATTN_ERR_UNSUPPORTED for B*h > 65535, otherwise as
+ * attn_fwd.
+ */
+attn_status_t attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int h, int T_q, int T_kv, int d, float scale, int causal,
+                             int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_naive_workspace_bytes -- bytes of the two materialised matrices of
+ * attn_fwd_naive: 4 * B * h * T_q * T_kv (0 for negative sizes).
+ */
+size_t attn_naive_workspace_bytes(int B, int h, int T_q, int T_kv);
 
 /*
  * attn_fwd_decode_noalloc -- the decode path (T_q == 1) without any
