@@ -1,19 +1,24 @@
 #!/usr/bin/env python
 """Benchmark of the exact-attention hot path on GB300.
 
-One step = one pass of the whole path over one batch of synthetic input:
-  1. causal prefill, GPT-2 shape: B=8, h=12, T=1024, d=64, bf16 (tensor-core
-     kernel), and
-  2. decode against a KV cache: B=32, h=12, T_q=1, T_kv=16384, d=64, bf16
+One step = one pass of the whole path over one batch of synthetic input,
+three calls of the library:
+  1. causal prefill, GPT-2 shape: B=8, h=12, T=1024, d=64, bf16,
+  2. causal prefill, very long: B=1, h=12, T=16384, d=64, fp16, inputs x0.5
+     (the largest prefill workload), and
+  3. decode against a KV cache: B=32, h=12, T_q=1, T_kv=16384, d=64, bf16
      (split-KV kernel + exact merge kernel).
+The two prefills run on the tensor cores; the decode streams the cache.
 
 Metric: the step's roofline time divided by its measured time, in percent.
-The roofline time of a kernel is max(FLOPs / tensor peak, bytes / HBM peak)
+The roofline time of a call is max(FLOPs / tensor peak, bytes / HBM peak)
 with the algorithmic FLOPs (4*d per visible query-key pair, causal pairs
 counted) and bytes (Q, K, V read once, O and lse written once); the peaks
 are the measured ones in MEASURED_PEAKS.json. `value` is whole-job
 throughput in units of one GB300's roofline: 100 * N * t_roof / t_step,
-so at N=1 it is the percentage of the roofline reached.
+so at N=1 it is the percentage of the roofline reached. Each call's own
+fraction is in `calls`, and every workload (the seven runs) is measured on
+its own, with an L2 flush between launches, in `runs`.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -47,7 +52,15 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "decode": os.path.join(ROOT, "exact_io_aware_attn_gb300", "csrc", "decode_sm103.cu"),
     "prefill": os.path.join(ROOT, "exact_io_aware_attn_gb300", "csrc", "prefill_sm103.cu"),
+    "prefill_very_long": os.path.join(ROOT, "exact_io_aware_attn_gb300", "csrc",
+                                      "prefill_sm103.cu"),
 }
+# repeats of the step after the timed K steps: >= 3 repeats of >= 20 steps
+REPEATS = 3
+REPEAT_MIN_STEPS = 20
+# per-workload timing: launches per repeat, repeats, warm-up launches
+RUN_LAUNCHES, RUN_REPEATS, RUN_WARMUP = 20, 3, 3
+L2_FLUSH_BYTES = 256 << 20      # twice the 129 MB L2
 
 
 def load_peaks():
@@ -79,35 +92,36 @@ def load_traffic(kind):
 
 
 # ----------------------------------------------------------------- work model
-def step_work():
+def step_calls():
+    """The step's calls: (key, workload, traffic key)."""
+    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL, VERY_LONG
+    return [("prefill_gpt2", GPT2_PREFILL, "prefill"),
+            ("prefill_very_long", VERY_LONG, "prefill_very_long"),
+            ("decode", DECODE, "decode")]
+
+
+def work_of(w, peaks):
+    """Algorithmic FLOPs and bytes of one call of workload w, its roofline
+    time and which roof binds."""
     from exact_io_aware_attn_gb300 import cost
-    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL
-    p, d = GPT2_PREFILL, DECODE
-    return {
-        "prefill_flops": cost.flops(p.B, p.h, p.T_q, p.T_kv, p.d, p.causal),
-        "prefill_bytes": cost.min_bytes(p.B, p.h, p.T_q, p.T_kv, p.d),
-        "decode_flops": cost.flops(d.B, d.h, d.T_q, d.T_kv, d.d, d.causal),
-        "decode_bytes": cost.min_bytes(d.B, d.h, d.T_q, d.T_kv, d.d),
-    }
-
-
-def roofline_times(work, peaks):
-    tc = peaks["bf16_tflops"] * 1e12
-    bw = peaks["hbm_gbs"] * 1e9
-    tp = max(work["prefill_flops"] / tc, work["prefill_bytes"] / bw)
-    td = max(work["decode_flops"] / tc, work["decode_bytes"] / bw)
-    return tp, td
+    fl = cost.flops(w.B, w.h, w.T_q, w.T_kv, w.d, w.causal)
+    by = cost.min_bytes(w.B, w.h, w.T_q, w.T_kv, w.d, h_kv=w.kv_heads)
+    t_tc = fl / (peaks["bf16_tflops"] * 1e12)
+    t_bw = by / (peaks["hbm_gbs"] * 1e9)
+    return {"flops": fl, "bytes": by, "t_roof": max(t_tc, t_bw),
+            "bound": "tensor" if t_tc >= t_bw else "hbm"}
 
 
 def config_block():
-    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL
+    calls = step_calls()
     return {
-        "workload": "gpt2_causal_prefill_B8_h12_T1024_d64_bf16 + decode_B32_h12_Tkv16384_d64_bf16",
-        "prefill": GPT2_PREFILL.describe(),
-        "decode": DECODE.describe(),
+        "workload": " + ".join(w.name for _, w, _ in calls),
+        **{key: w.describe() for key, w, _ in calls},
         "l2": "inputs larger than L2: each step streams the 1.61 GB KV cache, which also "
-              "evicts the 38 MB of prefill inputs before the next step",
-        "data": "synthetic N(0,1) from torch CPU generator seed 0, q then k then v",
+              "evicts the prefill inputs (38 MB and 75 MB) before the next step; the per-workload "
+              "runs flush L2 before every timed launch (a 256 MB write, then a 256 MB read)",
+        "data": "synthetic N(0,1) from torch CPU generator seed 0, q then k then v "
+                "(x0.5 for the very long prefill)",
     }
 
 
@@ -197,76 +211,122 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- CPU oracle
-def oracle_step_sample(inputs_cpu, n_prefill_heads, n_decode_rows):
-    """Time the float64 oracle on a bounded sample of one step. Returns
-    (seconds, fraction of the prefill heads, fraction of the decode rows)."""
+_INPUTS = {}
+
+
+def cached_inputs(w, one_head=False):
+    """make_workload(w) (CPU tensors), kept for reuse: drawing the decode
+    cache takes seconds. one_head: a single head of w's shape and
+    distribution (B = h = 1, same seed), for the oracle's row samples."""
+    import dataclasses
+
+    from exact_io_aware_attn_gb300.inputs import make_workload
+    key = (w.name, one_head)
+    if key not in _INPUTS:
+        _INPUTS[key] = make_workload(dataclasses.replace(w, B=1, h=1, h_kv=0) if one_head else w)
+    return _INPUTS[key]
+
+
+def oracle_sample(w, n_rows):
+    """Time the float64 oracle on n_rows query rows of workload w. Prefill:
+    the last n_rows rows of one head of w's shape and distribution (a causal
+    row sees as many keys as in the full problem). Decode: n_rows whole
+    (b, h) rows of the workload itself. Returns (seconds, rows, rows of the
+    whole call). The oracle forms each row's whole score vector, so its cost
+    per row does not depend on the mask: whole-call time = seconds * total /
+    rows."""
+    import numpy as np
+
     import oracle
-    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL
-    (pq, pk, pv), (dq, dk, dv) = inputs_cpu
-    scale = 0.125
+    if w.T_q == 1:
+        q, k, v = cached_inputs(w)
+        n_rows = max(1, min(n_rows, w.B * w.h))
+        t0 = time.perf_counter()
+        for i in range(n_rows):
+            b, h = divmod(i, w.h)
+            oracle.standard_attention(q[b, h].double().numpy(), k[b, h].double().numpy(),
+                                      v[b, h].double().numpy(), scale=w.scale, causal=False)
+        return time.perf_counter() - t0, n_rows, w.B * w.h
+    q, k, v = cached_inputs(w, one_head=True)
+    n_rows = max(1, min(n_rows, w.T_q))
+    rows = np.arange(w.T_q - n_rows, w.T_q)
+    qn, kn, vn = q[0, 0].double().numpy(), k[0, 0].double().numpy(), v[0, 0].double().numpy()
     t0 = time.perf_counter()
-    done = 0
-    for b in range(GPT2_PREFILL.B):
-        for h in range(GPT2_PREFILL.h):
-            if done == n_prefill_heads:
-                break
-            oracle.standard_attention(pq[b, h].double().numpy(), pk[b, h].double().numpy(),
-                                      pv[b, h].double().numpy(), scale=scale, causal=True)
-            done += 1
-    rows = 0
-    for b in range(DECODE.B):
-        for h in range(DECODE.h):
-            if rows == n_decode_rows:
-                break
-            oracle.standard_attention(dq[b, h].double().numpy(), dk[b, h].double().numpy(),
-                                      dv[b, h].double().numpy(), scale=scale, causal=False)
-            rows += 1
-    dt = time.perf_counter() - t0
-    return dt, done / (GPT2_PREFILL.B * GPT2_PREFILL.h), rows / (DECODE.B * DECODE.h)
+    oracle.standard_attention(qn, kn, vn, scale=w.scale, causal=w.causal, rows=rows)
+    return time.perf_counter() - t0, n_rows, w.B * w.h * w.T_q
 
 
-def make_inputs_cpu():
-    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL, make_workload
-    return make_workload(GPT2_PREFILL), make_workload(DECODE)
+def describe_sample(w, n):
+    blas = f"float64 numpy, BLAS threads {os.environ['OPENBLAS_NUM_THREADS']}"
+    if w.T_q == 1:
+        return f"{n} of {w.B * w.h} (b, h) decode rows, {blas}"
+    return (f"the last {n} query rows of one head of the same shape and distribution "
+            f"(of {w.B * w.h * w.T_q} rows in the call), {blas}")
 
 
-def cpu_baseline(inputs_cpu, peaks, prefill_heads=96, decode_rows=384):
-    work = step_work()
-    tp, td = roofline_times(work, peaks)
-    secs, fp, fd = oracle_step_sample(inputs_cpu, prefill_heads, decode_rows)
-    value = 100.0 * (fp * tp + fd * td) / secs
-    return {"value": value, "unit": UNIT, "cores": _CORES, "kind": "oracle",
-            "sample": f"{prefill_heads} of 96 prefill heads and {decode_rows} of 384 decode rows "
-                      f"of one step, float64 numpy (BLAS threads {os.environ['OPENBLAS_NUM_THREADS']})",
-            "seconds": secs}
+# oracle rows per workload for its timing (a second or so each), by T_q
+ORACLE_SAMPLE_ROWS = {1: 48, 256: 256, 1024: 1024, 4096: 512, 8192: 256, 16384: 128}
+
+
+def oracle_estimate(w):
+    """(seconds for the whole call, sample description) for the float64 oracle."""
+    secs, n, total = oracle_sample(w, ORACLE_SAMPLE_ROWS.get(w.T_q, 256))
+    return secs * total / n, describe_sample(w, n) + "; whole-call time scaled from the sample"
+
+
+def cpu_baseline(peaks, oracle_times):
+    """The oracle on the host cores for the whole step, from per-call row
+    samples (oracle_times: key -> (seconds per whole call, sample))."""
+    calls = step_calls()
+    t_roof = sum(work_of(w, peaks)["t_roof"] for _, w, _ in calls)
+    secs = sum(oracle_times[key][0] for key, _, _ in calls)
+    return {"value": 100.0 * t_roof / secs, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+            "sample": "; ".join(f"{key}: {oracle_times[key][1]}" for key, _, _ in calls),
+            "seconds_per_step": secs}
 
 
 # ----------------------------------------------------------------- reference arm
 def run_reference(args):
     """The oracle, as it stands, on the host cores: each step is a bounded
-    sample of the step's work (whole prefill heads and whole decode rows),
-    sized so that warm-up + timed steps take about a minute and a half."""
+    sample of the step's three calls (query rows of the prefills, whole
+    decode rows), sized so that warm-up + timed steps take a minute or two."""
     rank, world, _ = dist_init(args.gpus)
     if rank != 0:
         return 0
     peaks = load_peaks()
-    inputs_cpu = make_inputs_cpu()
-    unit_s, _, _ = oracle_step_sample(inputs_cpu, 1, 1)        # calibration unit
-    per_step = 90.0 / max(1, args.steps + args.warmup)
-    units = int(max(1, min(8, per_step // max(unit_s, 1e-6))))
-    heads, rows = units, units
+    calls = step_calls()
+    # calibration: seconds per sampled row of each call, on samples of the
+    # size the steps use at most (the oracle's matrices grow with the rows)
+    per_row = {}
+    for key, w, _ in calls:
+        oracle_sample(w, 4)                                   # first touch
+        secs, n, total = oracle_sample(w, max(1, ORACLE_SAMPLE_ROWS.get(w.T_q, 256) // 4))
+        per_row[key] = (secs / n, total)
+    budget = 90.0 / max(1, args.steps + args.warmup)        # seconds per step
+    share = budget / len(calls)
+    rows = {key: int(max(1, min(total, ORACLE_SAMPLE_ROWS.get(w.T_q, 256),
+                                share // max(per_row[key][0], 1e-6))))
+            for key, w, _ in calls}
+
+    def one_step():
+        """Seconds the oracle would take for the whole step: each call's
+        sampled rows timed and scaled to all of its rows."""
+        t = 0.0
+        for key, w, _ in calls:
+            secs, n, total = oracle_sample(w, rows[key])
+            rows[key] = n
+            t += secs * total / n
+        return t
+
     for _ in range(args.warmup):
-        oracle_step_sample(inputs_cpu, heads, rows)
-    tot, fp, fd = 0.0, 0.0, 0.0
-    for _ in range(args.steps):
-        secs, fp, fd = oracle_step_sample(inputs_cpu, heads, rows)
-        tot += secs
-    work = step_work()
-    tp, td = roofline_times(work, peaks)
+        one_step()
+    tot = sum(one_step() for _ in range(args.steps))
     per_step_s = tot / max(1, args.steps)
-    value = 100.0 * (fp * tp + fd * td) / per_step_s
-    sample = (f"each step: {heads} of 96 prefill heads and {rows} of 384 decode rows, "
-              f"float64 numpy (BLAS threads {os.environ['OPENBLAS_NUM_THREADS']})")
+    roof = sum(work_of(w, peaks)["t_roof"] for _, w, _ in calls)
+    value = 100.0 * roof / per_step_s
+    sample = ("each step: " + "; ".join(f"{key}: {describe_sample(w, rows[key])}"
+                                        for key, w, _ in calls)
+              + "; each call's time scaled from its sampled rows to the whole call")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_s * 1e3,
@@ -281,11 +341,88 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- our arm
+def time_launches(call, stream, flush=None, n=RUN_LAUNCHES, reps=RUN_REPEATS, warmup=RUN_WARMUP):
+    """Per-launch CUDA-event times (ms) of `call` on `stream`: `reps` repeats
+    of `n` launches, each launch bracketed by its own events with an L2
+    flush before it (outside the events). Returns the mean of each repeat."""
+    import torch
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    means = []
+    for _ in range(reps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            if flush is not None:
+                flush()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        means.append(sum(a.elapsed_time(b) for a, b in ev) / n)
+    return means
+
+
+def measure_runs(dev, stream, peaks, with_oracle):
+    """Every workload on its own: kernel, time per call, throughput and
+    fractions of the two roofs, and the oracle's time for the same call."""
+    import torch
+
+    from exact_io_aware_attn_gb300 import _lib
+    from exact_io_aware_attn_gb300.inputs import WORKLOADS
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        # write a buffer twice the size of L2 (evicts the inputs), then read
+        # another one (evicts the written lines, so no write-back of them
+        # lands inside the timed launch)
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_out)
+    runs = {}
+    for w in WORKLOADS:
+        q, k, v = (t.to(dev) for t in cached_inputs(w))
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+        def call():
+            _lib.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse, stream=stream)
+        means = time_launches(call, stream, flush=flush)
+        st, word = _lib.get_device_error()
+        if st != _lib.ATTN_OK:
+            raise SystemExit(f"device status {st} ({word:#x}) in workload {w.name}")
+        ms = statistics.median(means)
+        wk = work_of(w, peaks)
+        tflops = wk["flops"] / (ms * 1e-3) / 1e12
+        gbs = wk["bytes"] / (ms * 1e-3) / 1e9
+        entry = {
+            "kernel": _lib.last_kernel_name(), "us_per_call": ms * 1e3,
+            "repeats_us": [m * 1e3 for m in means],
+            "spread_pct": 100.0 * (max(means) - min(means)) / ms,
+            "tflops": tflops, "gbs": gbs,
+            "frac_tensor_peak": tflops / peaks["bf16_tflops"],
+            "frac_tensor_peak_sustained": tflops / peaks["bf16_tflops_sustained"],
+            "frac_hbm_peak": gbs / peaks["hbm_gbs"],
+            "bound": wk["bound"], "frac_of_roofline": wk["t_roof"] / (ms * 1e-3),
+            "flops": wk["flops"], "bytes": wk["bytes"],
+        }
+        if with_oracle:
+            secs, sample = oracle_estimate(w)
+            entry["oracle_s_per_call"] = secs
+            entry["oracle_sample"] = sample
+        runs[w.name] = entry
+        del q, k, v, o, lse
+    del flush_w, flush_r, flush_out
+    torch.cuda.empty_cache()
+    return runs
+
+
 def run_ours(args):
     import torch
 
     from exact_io_aware_attn_gb300 import _lib, build as build_mod
-    from exact_io_aware_attn_gb300.inputs import DECODE, GPT2_PREFILL
 
     rank, world, local = dist_init(args.gpus)
     if not torch.cuda.is_available():
@@ -294,20 +431,24 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     build_mod.build()
     peaks = load_peaks()
-    work = step_work()
-    tp_roof, td_roof = roofline_times(work, peaks)
+    calls = step_calls()
+    works = {key: work_of(w, peaks) for key, w, _ in calls}
 
-    inputs_cpu = make_inputs_cpu()
-    (pq, pk, pv), (dq, dk, dv) = [[t.to(dev) for t in grp] for grp in inputs_cpu]
-    po = torch.empty_like(pq)
-    plse = torch.empty(pq.shape[:3], dtype=torch.float32, device=dev)
-    do = torch.empty_like(dq)
-    dlse = torch.empty(dq.shape[:3], dtype=torch.float32, device=dev)
+    inputs_cpu = {key: cached_inputs(w) for key, w, _ in calls}
+    dev_in = {key: [t.to(dev) for t in grp] for key, grp in inputs_cpu.items()}
+    outs = {key: (torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device=dev))
+            for key, (q, _, _) in dev_in.items()}
+    causal = {key: w.causal for key, w, _ in calls}
     stream = torch.cuda.current_stream(dev)
 
+    def launch(key):
+        q, k, v = dev_in[key]
+        o, lse = outs[key]
+        _lib.attn_fwd(q, k, v, causal=causal[key], out=o, lse=lse, stream=stream)
+
     def step():
-        _lib.attn_fwd(pq, pk, pv, causal=True, out=po, lse=plse)
-        _lib.attn_fwd(dq, dk, dv, causal=False, out=do, lse=dlse)
+        for key, _, _ in calls:
+            launch(key)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -315,64 +456,71 @@ def run_ours(args):
     st, word = _lib.get_device_error()
     if st != _lib.ATTN_OK:
         raise SystemExit(f"device status {st} ({word:#x}) after warm-up")
-    kernels = {"prefill": None, "decode": None}
-    _lib.attn_fwd(pq, pk, pv, causal=True, out=po, lse=plse)
-    kernels["prefill"] = _lib.last_kernel_name()
-    _lib.attn_fwd(dq, dk, dv, causal=False, out=do, lse=dlse)
-    kernels["decode"] = _lib.last_kernel_name()
-    splits = _lib.decode_num_splits(DECODE.B, DECODE.h, DECODE.T_kv, DECODE.d)
+    kernels = {}
+    for key, _, _ in calls:
+        launch(key)
+        kernels[key] = _lib.last_kernel_name()
+    launches_per_step = sum(2 if "+" in name else 1 for name in kernels.values())
+    torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    n_calls = len(calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 1)] for _ in range(K)]
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize()
         for i in range(K):
             ev[i][0].record(stream)
-            _lib.attn_fwd(pq, pk, pv, causal=True, out=po, lse=plse)
-            ev[i][1].record(stream)
-            _lib.attn_fwd(dq, dk, dv, causal=False, out=do, lse=dlse)
-            ev[i][2].record(stream)
+            for c, (key, _, _) in enumerate(calls):
+                launch(key)
+                ev[i][c + 1].record(stream)
         torch.cuda.synchronize()
         barrier(world)
+        # repeats: >= 3 back-to-back loops of >= 20 steps each, after the
+        # timed K steps (whatever K is)
+        rep_steps = max(REPEAT_MIN_STEPS, K)
+        rep_ev = []
+        for _ in range(REPEATS):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(rep_steps):
+                step()
+            b.record(stream)
+            rep_ev.append((a, b))
+        torch.cuda.synchronize()
     st, word = _lib.get_device_error()
     if st != _lib.ATTN_OK:
         raise SystemExit(f"device status {st} ({word:#x}) in the timed region")
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    pre_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
-    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][n_calls])
+    call_ms = {key: sum(e[c].elapsed_time(e[c + 1]) for e in ev) / K
+               for c, (key, _, _) in enumerate(calls)}
     step_ms = max_over_ranks(total_ms / K, world, dev)
-    # the K steps as 5 back-to-back repeats (>= 20 steps each at the default K):
-    # median and spread of the per-repeat step time
-    R = 5 if K >= 5 else 1
-    per = K // R
-    rep_ms = [ev[r * per][0].elapsed_time(ev[r * per + per - 1][2]) / per for r in range(R)]
-    repeats = {"n": R, "steps_each": per, "ms_per_step_median": statistics.median(rep_ms),
+    rep_ms = [a.elapsed_time(b) / rep_steps for a, b in rep_ev]
+    repeats = {"n": REPEATS, "steps_each": rep_steps,
+               "ms_per_step": rep_ms, "ms_per_step_median": statistics.median(rep_ms),
                "spread_pct": 100.0 * (max(rep_ms) - min(rep_ms)) / statistics.median(rep_ms)}
 
     # end to end through the public API with host buffers: pinned H2D of the
-    # step's inputs, the two calls, D2H of both outputs, every step
-    host_in = [[t.pin_memory() for t in grp] for grp in inputs_cpu]
-    host_out = [torch.empty(po.shape, dtype=po.dtype).pin_memory(),
-                torch.empty(plse.shape, dtype=torch.float32).pin_memory(),
-                torch.empty(do.shape, dtype=do.dtype).pin_memory(),
-                torch.empty(dlse.shape, dtype=torch.float32).pin_memory()]
-    h2d = sum(t.numel() * t.element_size() for grp in host_in for t in grp)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
-
+    # step's inputs, the three calls, D2H of every output, every step
+    host_in = {key: [t.pin_memory() for t in grp] for key, grp in inputs_cpu.items()}
+    host_out = {key: (torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                      torch.empty(lse.shape, dtype=torch.float32).pin_memory())
+                for key, (o, lse) in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for grp in host_in.values() for t in grp)
+    d2h = sum(t.numel() * t.element_size() for pair in host_out.values() for t in pair)
     # the C-ABI host-buffer entry: it copies the inputs in, runs the same
     # kernels on its device region, and copies o and lse out, in stream order
-    bufs = []
-    for grp in host_in:
+    bufs = {}
+    for key, grp in host_in.items():
         B_, h_, T_q_, d_ = grp[0].shape
         nbytes = _lib.host_buffer_bytes(B_, h_, grp[1].shape[1], T_q_, grp[1].shape[2], d_)
-        bufs.append(torch.empty(nbytes, dtype=torch.uint8, device=dev))
+        bufs[key] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        _lib.attn_fwd_host(*host_in[0], causal=True, out=host_out[0], lse=host_out[1],
-                           device_buffer=bufs[0], stream=stream, synchronize=False)
-        _lib.attn_fwd_host(*host_in[1], causal=False, out=host_out[2], lse=host_out[3],
-                           device_buffer=bufs[1], stream=stream, synchronize=False)
+        for key, _, _ in calls:
+            o_h, lse_h = host_out[key]
+            _lib.attn_fwd_host(*host_in[key], causal=causal[key], out=o_h, lse=lse_h,
+                               device_buffer=bufs[key], stream=stream, synchronize=False)
 
     e2e_steps = min(K, 20)
     for _ in range(3):
@@ -384,53 +532,86 @@ def run_ours(args):
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, world, dev)
+    del bufs, host_in, host_out
+    del dev_in, outs
+    torch.cuda.empty_cache()
 
     if rank != 0:
         return 0
 
-    roof_step = tp_roof + td_roof
+    with_oracle = world == 1 and not args.no_cpu_baseline
+    runs = measure_runs(dev, stream, peaks, with_oracle) if not args.no_runs else None
+
+    roof_step = sum(wk["t_roof"] for wk in works.values())
     value = 100.0 * world * roof_step / (step_ms * 1e-3)
     e2e_value = 100.0 * world * roof_step / (e2e_ms * 1e-3)
-    dec_gbs = work["decode_bytes"] / (dec_ms * 1e-3) / 1e9
-    pre_tflops = work["prefill_flops"] / (pre_ms * 1e-3) / 1e12
-    pre_gbs = work["prefill_bytes"] / (pre_ms * 1e-3) / 1e9
     peak_note = "of measured" if peaks["source"] == "measured" else "of fallback"
+    call_lines = {}
+    for key, w, tkey in calls:
+        wk, ms = works[key], call_ms[key]
+        tflops = wk["flops"] / (ms * 1e-3) / 1e12
+        gbs = wk["bytes"] / (ms * 1e-3) / 1e9
+        call_lines[key] = {
+            "workload": w.name, "kernel": kernels[key], "bound": wk["bound"],
+            "ms_per_launch": ms, "tflops": tflops, "gbs": gbs,
+            "frac_tensor_peak": tflops / peaks["bf16_tflops"],
+            "frac_hbm_peak": gbs / peaks["hbm_gbs"],
+            "frac_of_roofline": wk["t_roof"] / (ms * 1e-3),
+            "share_of_step": ms / (total_ms / K),
+            "algorithmic_flops_per_launch": wk["flops"],
+            "algorithmic_bytes_per_launch": wk["bytes"],
+            "traffic": load_traffic(tkey),
+        }
+    # the dominant kernel: the call with the largest share of the step
+    dom = max(call_lines, key=lambda key: call_lines[key]["ms_per_launch"])
+    dl = call_lines[dom]
+    if dl["bound"] == "tensor":
+        roofline = {"bound": "tensor", "achieved": dl["tflops"], "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": dl["tflops"] / peaks["bf16_tflops"]}
+    else:
+        roofline = {"bound": "hbm", "achieved": dl["gbs"], "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": dl["gbs"] / peaks["hbm_gbs"]}
+    roofline.update({"traffic": dl["traffic"], "kernel": f"{dom}: {dl['kernel']}",
+                     "peak_kind": peak_note + " (burst)",
+                     "algorithmic_flops_per_launch": dl["algorithmic_flops_per_launch"],
+                     "algorithmic_bytes_per_launch": dl["algorithmic_bytes_per_launch"],
+                     "ms_per_launch": dl["ms_per_launch"]})
+    dec = call_lines["decode"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f16", "data": "synthetic",
         "config": config_block(),
         "parallelism": "replicas only" if world > 1 else "single GPU",
-        "kernels": kernels, "decode_splits": splits,
-        "roofline": {"bound": "hbm", "kernel": "decode (split + merge)", "achieved": dec_gbs,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
-                     "traffic": load_traffic("decode"), "peak_kind": peak_note,
-                     "algorithmic_bytes_per_launch": work["decode_bytes"],
-                     "ms_per_launch": dec_ms},
-        "roofline_prefill": {
-            "bound": "hbm" if work["prefill_flops"] / work["prefill_bytes"] <
-                     peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9) else "tensor",
-            "kernel": kernels["prefill"], "achieved_tflops": pre_tflops,
-            "tensor_peak_tflops": peaks["bf16_tflops"],
-            "frac_of_tensor_peak": pre_tflops / peaks["bf16_tflops"],
-            "achieved_gbs": pre_gbs, "frac_of_roofline": tp_roof / (pre_ms * 1e-3),
-            "traffic": load_traffic("prefill"), "peak_kind": peak_note,
-            "algorithmic_flops_per_launch": work["prefill_flops"],
-            "algorithmic_bytes_per_launch": work["prefill_bytes"], "ms_per_launch": pre_ms},
+        "roofline": roofline,
+        "roofline_decode": {"bound": "hbm", "achieved": dec["gbs"], "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": dec["gbs"] / peaks["hbm_gbs"],
+                            "traffic": dec["traffic"], "kernel": dec["kernel"],
+                            "peak_kind": peak_note},
+        "calls": call_lines,
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps},
-        "gpu_launches": 3 * K,
+        "gpu_launches": launches_per_step * K,
+        "gpu_launches_note": f"{launches_per_step} per step (two prefill kernels, the decode's "
+                             "split and merge kernels) x K timed steps",
         "repeats": repeats,
         # device memory the library needs beyond the caller's inputs and
         # outputs: the decode's split partials (stream-ordered, per call); the
-        # prefill needs none (the T x T scores never exist)
-        "extra_device_bytes": {"prefill": 0, "decode": _lib.workspace_bytes(
-            DECODE.B, DECODE.h, DECODE.T_q, DECODE.T_kv, DECODE.d, 0)},
-        "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source")},
+        # prefills need none (the T x T scores never exist)
+        "extra_device_bytes": {"prefill_gpt2": 0, "prefill_very_long": 0,
+                               "decode": _lib.workspace_bytes(
+                                   calls[2][1].B, calls[2][1].h, calls[2][1].T_q,
+                                   calls[2][1].T_kv, calls[2][1].d, 0)},
+        "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained",
+                                        "source")},
+        "runs": runs,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inputs_cpu, peaks)
+    if with_oracle and runs is not None:
+        by_name = {r: runs[r] for r in runs}
+        oracle_times = {key: (by_name[w.name]["oracle_s_per_call"],
+                              by_name[w.name]["oracle_sample"]) for key, w, _ in calls}
+        line["cpu_baseline"] = cpu_baseline(peaks, oracle_times)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -549,6 +730,72 @@ def run_kernel_case(args):
     return 0
 
 
+def run_naive_table(args):
+    """The pages' comparison on GB300: causal attention of B=1, h=12, d=64,
+    fp16 heads at T = 512 ... 16384, the IO-aware forward (attn_fwd) beside
+    the materialising baseline (attn_fwd_naive, which writes the T x T score
+    and probability matrices to device memory). Per T: CUDA-event time per
+    call (L2 flushed before each launch), and the device bytes each call
+    needs beyond its inputs (outputs plus library workspace). Prints one
+    JSON line."""
+    import torch
+
+    from exact_io_aware_attn_gb300 import _lib, build as build_mod
+    from exact_io_aware_attn_gb300.inputs import F16, make_qkv
+
+    build_mod.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_out)
+
+    B, h, d = 1, 12, 64
+    rows = []
+    for T in (512, 1024, 2048, 4096, 8192, 16384):
+        q, k, v = (t.to(dev) for t in make_qkv(B, h, T, T, d, F16, 1.0, 0))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, h, T), dtype=torch.float32, device=dev)
+        out_bytes = o.numel() * 2 + lse.numel() * 4
+        io_ws = _lib.splitkv_workspace_bytes(B, h, T, T, d, 0)
+
+        def io_call():
+            _lib.attn_fwd(q, k, v, causal=True, out=o, lse=lse, stream=stream)
+        io_ms = statistics.median(time_launches(io_call, stream, flush=flush))
+        io_name = _lib.last_kernel_name()
+        o_io = o.clone()
+        nb = _lib.naive_workspace_bytes(B, h, T, T)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+        def naive_call():
+            _lib.attn_fwd_naive(q, k, v, causal=True, out=o, lse=lse, workspace=ws, stream=stream)
+        naive_ms = statistics.median(time_launches(naive_call, stream, flush=flush, n=10))
+        st, word = _lib.get_device_error()
+        if st != _lib.ATTN_OK:
+            raise SystemExit(f"device status {st} ({word:#x}) at T={T}")
+        diff = float((o.float() - o_io.float()).abs().max())
+        rows.append({"T": T, "io_aware_kernel": io_name, "io_aware_us": io_ms * 1e3,
+                     "naive_kernel": _lib.last_kernel_name(), "naive_us": naive_ms * 1e3,
+                     "speedup": naive_ms / io_ms,
+                     "io_aware_bytes_beyond_inputs": out_bytes + io_ws,
+                     "naive_bytes_beyond_inputs": out_bytes + nb,
+                     "memory_ratio": (out_bytes + nb) / (out_bytes + io_ws),
+                     "max_abs_diff_o": diff})
+        del q, k, v, o, lse, ws, o_io
+        torch.cuda.empty_cache()
+    by_t = {r["T"]: r for r in rows}
+    print(json.dumps({"table": "io_aware_vs_naive", "B": B, "h": h, "d": d, "dtype": "f16",
+                      "causal": True, "rows": rows,
+                      "speedup_at_8192": by_t[8192]["speedup"],
+                      "memory_ratio_at_16384": by_t[16384]["memory_ratio"]}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[1])
     ap.add_argument("--gpus", type=int, default=1)
@@ -556,6 +803,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-runs", action="store_true",
+                    help="skip the per-workload measurements (and with them the oracle timing)")
     ap.add_argument("--kernel-case", metavar="prefill|decode|WORKLOAD",
                     help="profiling mode: run only this call of the step, or a named workload")
     ap.add_argument("--case-batch", type=int, default=None,
@@ -568,9 +817,14 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=None,
                     help="with a prefill --kernel-case: attn_fwd_splitkv with this many key "
                          "partitions (1 = unsplit; 0 = the library's choice)")
+    ap.add_argument("--naive-table", action="store_true",
+                    help="time the IO-aware forward beside the materialising baseline at "
+                         "T = 512 ... 16384 (B 1, h 12, d 64, fp16, causal)")
     ap.add_argument("--var-len", action="store_true",
                     help="with --page-size: sequence lengths uniform in [T/4, T]")
     args = ap.parse_args(argv)
+    if args.naive_table:
+        return run_naive_table(args)
     if args.kernel_case:
         return run_kernel_case(args)
     if args.impl == "reference":
