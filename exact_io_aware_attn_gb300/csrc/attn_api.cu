@@ -678,6 +678,9 @@ size_t attn_gqa_workspace_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int
   if (B < 0 || h_q < 0 || h_kv < 1 || T_q < 0 || T_kv < 0 || (d != 64 && d != 128)) return 0;
   if (h_q % h_kv != 0) return 0;
   if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+  // groups of 4 or more decode on the tensor cores, which take 1..64
+  // partitions (attn_fwd_gqa rejects more as unsupported)
+  if (gqa_decode_on_tensor_cores(h_q, h_kv) && num_splits > 64) return 0;
   if (T_q != 1 || B == 0 || h_q == 0 || T_kv < 1) return 0;
   const int splits = num_splits > 0 ? num_splits : auto_splits(B, h_q, h_kv, T_kv, d);
   return ws_bytes(B, h_q, d, splits);

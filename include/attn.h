@@ -125,6 +125,9 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
  * stream-ordered allocator as attn_fwd does. The decode path reads each
  * cached key/value row once for up to 8 query heads of its group.
  * h_kv == h_q is plain attention (same kernels as attn_fwd_ex).
+ * Groups of 4 or more query heads per key/value head decode on the tensor
+ * cores with 1..64 partitions: num_splits 65..1024 then returns
+ * ATTN_ERR_UNSUPPORTED (0, the library's choice, always stays in range).
  * Returns ATTN_ERR_INVALID_ARG if h_kv < 1 or h_q is not a multiple of h_kv.
  */
 attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -136,6 +139,8 @@ attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o,
  * attn_gqa_workspace_bytes -- workspace attn_fwd_gqa needs (0 for the
  * prefill path or invalid sizes): B*h_q*S*(d+4)*4 bytes, S the partition
  * count (num_splits, or the library's choice for this grouping when 0).
+ * Returns 0 for a split count attn_fwd_gqa would reject (above 64 for groups
+ * of 4 or more).
  */
 size_t attn_gqa_workspace_bytes(int B, int h_q, int h_kv, int T_q, int T_kv, int d,
                                 int num_splits);

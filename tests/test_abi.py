@@ -211,6 +211,24 @@ def test_gqa_workspace_bytes(L):
     assert _lib.gqa_workspace_bytes(2, 8, 8, 1, 300, 64, 0) == _lib.workspace_bytes(2, 8, 1, 300, 64, 0)
 
 
+@pytest.mark.parametrize("h_q,h_kv", [(8, 2), (16, 2), (8, 4), (12, 12)])
+@pytest.mark.parametrize("splits", [1, 16, 64, 65, 200, 1024])
+def test_gqa_workspace_query_agrees_with_the_call(L, h_q, h_kv, splits):
+    """The workspace query reports 0 exactly for the split counts the call
+    rejects (on the tensor-core path, above 64; the rejection happens before
+    any CUDA call), and the partials' size otherwise."""
+    nbytes = _lib.gqa_workspace_bytes(2, h_q, h_kv, 1, 3000, 64, splits)
+    if h_q // h_kv >= 4 and splits > 64:
+        assert nbytes == 0
+        # fake addresses 2^40 apart: no tensor overlaps another
+        q, k, v, o, lse, ws = ((1 << 40) * i for i in range(1, 7))
+        st = _lib.fwd_gqa_raw(q, k, v, o, lse, 2, h_q, h_kv, 1, 3000, 64, 0.125, 0,
+                              _lib.ATTN_BF16, splits, ws, 1 << 30, None)
+        assert st == _lib.ATTN_ERR_UNSUPPORTED
+    else:
+        assert nbytes == 2 * h_q * splits * 68 * 4
+
+
 # backward: fake addresses for the extra tensors, spaced like the others
 DO, DQ, DK, DV = (0x100000 * i for i in range(7, 11))
 
