@@ -411,9 +411,12 @@ int paged_ctas_per_sm(int d) {
 // block table can name (the lengths live on the device).
 int paged_auto_splits(int B, int h_q, int h_kv, int d, int page_size, int max_pages) {
   const long long t = std::min<long long>(0x7fffffffll, static_cast<long long>(page_size) * max_pages);
-  if (paged_on_tensor_cores(h_q, h_kv, page_size))  // one prefill CTA per SM
-    return std::min(64, attn::detail::choose_splits_cap(static_cast<long long>(B) * h_kv,
-                                                        static_cast<int>(t), sm_count()));
+  if (paged_on_tensor_cores(h_q, h_kv, page_size)) {  // one prefill CTA per SM, per unit of heads
+    const long long bh = static_cast<long long>(B) * h_kv;
+    const long long units =
+        attn::paged_head_pairs(d, h_q / h_kv, bh, page_size) ? (bh + 1) / 2 : bh;
+    return std::min(64, attn::detail::choose_splits_cap(units, static_cast<int>(t), sm_count()));
+  }
   const long long cap = static_cast<long long>(sm_count()) * paged_ctas_per_sm(d);
   return attn::detail::choose_splits_cap(static_cast<long long>(B) * h_q, static_cast<int>(t), cap);
 }

@@ -108,9 +108,15 @@ inline int decode_heads_per_cta(int group) { return (group % 2 == 0) ? 2 : 1; }
 // The tensor-core forward pairs two heads per work unit (each with its own
 // query tile and key/value stream) when a head has at most 128 query rows at
 // d = 64, so that both tiles of a unit exist; its units are then
-// ceil(B*h / 2) per key partition instead of B*h. (Contiguous K/V only: the
-// paged mode keeps one head per unit.)
+// ceil(B*h / 2) per key partition instead of B*h (contiguous or paged K/V).
 inline bool head_pair_mode(int d, int T_q, long long BH) { return d == 64 && T_q <= 128 && BH >= 2; }
+// With a paged cache, head pairs pay off for pages of 64 rows or more (one
+// or two boxes per key tile and head); with smaller pages the producer warp's
+// many box copies per key tile set the pace and one head per unit keeps more,
+// smaller units (measured: 16-row pages no faster, variable lengths slower).
+inline bool paged_head_pairs(int d, int T_q, long long BH, int page_size) {
+  return head_pair_mode(d, T_q, BH) && page_size >= 64;
+}
 
 // Split kernel occupancy (CTAs per SM) for the split-count heuristic.
 int decode_split_ctas_per_sm(int d, int heads_per_cta);

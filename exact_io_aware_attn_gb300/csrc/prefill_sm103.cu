@@ -102,6 +102,15 @@ struct Cfg {
   static constexpr bool SEP_P = (D == 64);
 };
 
+// Head pairs with a paged cache: at the start of each unit the producer
+// copies the unit's block-table entries (per tile, the pages its key range
+// touches) into shared memory, so the page of every box is a shared-memory
+// read, not a dependent global load per box in the producer's path. (Copying
+// the next unit's entries ahead of time was measured slower.) Key ranges that
+// need more entries than the buffer holds read the table per box instead.
+constexpr int kTblEntries = 2048;
+constexpr int kTblBytes = 2 * kTblEntries * 4;  // [tile][entry]
+
 __host__ __device__ constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
 template <int D>
 __host__ __device__ constexpr uint32_t col_o(int x) {
@@ -266,7 +275,7 @@ __device__ __forceinline__ int unit_of_round(int r, int bid, int G) {
   return (r & 1) ? r * G + (G - 1 - bid) : r * G + bid;
 }
 
-// HP: head-pair mode (two heads per unit, contiguous K/V, d = 64 only).
+// HP: head-pair mode (two heads per unit, d = 64 only).
 template <int D, bool BF16, bool PAGED, bool HP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    float* __restrict__ lse, int T_q, int T_kv, int BH, int n_pairs,
                    float scale_log2, int causal, unsigned int* __restrict__ status, int h_q,
                    int h_kv, int S, float* __restrict__ part, const PagedKV pkv) {
-  static_assert(!HP || (D == 64 && !PAGED), "head pairs: d = 64, contiguous K/V");
+  static_assert(!HP || D == 64, "head pairs: d = 64");
   using C = Cfg<D>;
   constexpr int SL = C::SLOTS;
   extern __shared__ uint8_t smem_raw[];
@@ -293,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_free = mma_done + 1;   // SEP_P: softmax X has read S_X (128 arrivals)
   uint64_t* pv_done = s_free + 2;    // SEP_P: PV_X complete (P_X and O_X free)
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMPTR);
+  // (paged head pairs only) the staged block-table entries of tiles A and B
+  int* tbl = reinterpret_cast<int*>(smem + C::OFF_TMEMPTR + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -440,6 +451,95 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile it belongs to has no key tile j (then the slot gets no data
             // and its full barrier just completes, keeping the phases in step).
             const int nt = w.rows_b > 0 ? 2 : 1;
+            if constexpr (PAGED) {
+              // Paged cache: the whole warp runs this loop (waits made
+              // warp-uniform); lane i copies box i of each key tile. First
+              // the unit's table entries: for tile t, the pages holding keys
+              // [j0 * kBN, min(length, (j0 + n_t) * kBN)) -- only entries a
+              // valid key uses are read (and checked).
+              int p_lo[2] = {0, 0};
+              bool staged = true;
+              for (int t = 0; t < nt; ++t) {
+                const int n_t = t ? w.n_b : w.n_a;
+                const int b = (t ? w.bh_b : w.bh) / h_q;
+                const int k_end = min(t ? w.tkv_b : w.tkv, (w.j0 + n_t) * kBN);
+                const int lo = (w.j0 * kBN) >> pkv.page_shift;
+                const int cnt = k_end > w.j0 * kBN ? ((k_end - 1) >> pkv.page_shift) + 1 - lo : 0;
+                p_lo[t] = lo;
+                if (cnt > kTblEntries) {
+                  staged = false;
+                  continue;
+                }
+                for (int i = lane; i < cnt; i += 32) {
+                  int pg = __ldg(pkv.table + static_cast<size_t>(b) * pkv.max_pages + lo + i);
+                  if (static_cast<unsigned>(pg) >= static_cast<unsigned>(pkv.num_pages)) {
+                    atomicCAS(status, 0u,
+                              status_word_code(1u /* ATTN_ERR_INVALID_ARG */, kKernPrefill,
+                                               kSiteBadPage));
+                    pg = 0;
+                  }
+                  tbl[t * kTblEntries + i] = pg;
+                }
+              }
+              __syncwarp();
+              const int rows = min(1 << pkv.page_shift, kBN);
+              for (int j = 0; ok && j < w.n_all; ++j) {
+                for (int kind = 0; ok && kind < 2; ++kind) {
+                  for (int t = 0; ok && t < nt; ++t) {
+                    const uint32_t slot = g % SL;
+                    ok = uniform(ptx::mbar_wait(&slot_empty[slot], ((g / SL) & 1) ^ 1, status,
+                                                status_word(kKernPrefill, kSiteProdSlot)));
+                    if (!ok) break;
+                    const bool skip = j >= (t ? w.n_b : w.n_a);
+                    if (skip) {
+                      // no data: the full barrier just completes, and this
+                      // thread releases the slot for both tiles
+                      if (lead) {
+                        ptx::mbar_arrive(&slot_full[slot]);
+                        ptx::mbar_arrive(&slot_empty[slot]);
+                        ptx::mbar_arrive(&slot_empty[slot]);
+                      }
+                    } else {
+                      if (lead) ptx::mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
+                      // the copies start after the lead lane has announced the bytes
+                      __syncwarp();
+                      uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+                      const int bh_t = t ? w.bh_b : w.bh;
+                      const int b = bh_t / h_q;
+                      const int kvh = bh_t - b * h_q;
+                      const int i = lane * rows;
+                      const int key = (w.j0 + j) * kBN + i;
+                      if (i < kBN) {
+                        int pg = 0;  // rows past the length: page 0, masked later
+                        if (key < (t ? w.tkv_b : w.tkv)) {
+                          if (staged) {
+                            pg = tbl[t * kTblEntries + (key >> pkv.page_shift) - p_lo[t]];
+                          } else {
+                            pg = __ldg(pkv.table + static_cast<size_t>(b) * pkv.max_pages +
+                                       (key >> pkv.page_shift));
+                            if (static_cast<unsigned>(pg) >= static_cast<unsigned>(pkv.num_pages)) {
+                              atomicCAS(status, 0u,
+                                        status_word_code(1u /* ATTN_ERR_INVALID_ARG */,
+                                                         kKernPrefill, kSiteBadPage));
+                              pg = 0;
+                            }
+                          }
+                        }
+                        ptx::tma_load_3d(dst + i * 128, kind ? &tmV : &tmK, &slot_full[slot], 0,
+                                         key & ((1 << pkv.page_shift) - 1), pg * h_q + kvh, pol_kv);
+                      }
+                      // the stand-in release for the other tile
+                      if (lead) ptx::mbar_arrive(&slot_empty[slot]);
+                    }
+                    ++g;
+                  }
+                }
+              }
+              // every lane is done with the staged entries before the next
+              // unit overwrites them
+              __syncwarp();
+              continue;
+            }
             for (int j = 0; ok && j < w.n_all; ++j) {
               for (int kind = 0; ok && kind < 2; ++kind) {
                 for (int t = 0; ok && t < nt; ++t) {
@@ -933,6 +1033,7 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t strea
                      const PagedKV& pkv, const void* k_pool, const void* v_pool) {
   using C = Cfg<D>;
   auto kern = prefill_kernel<D, BF16, PAGED, HP>;
+  constexpr int smem_bytes = C::SMEM_BYTES + ((PAGED && HP) ? kTblBytes : 0);
   static std::mutex mu;
   static uint64_t configured = 0;  // one bit per device ordinal
   int dev = 0;
@@ -941,7 +1042,7 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t strea
   {
     std::lock_guard<std::mutex> g(mu);
     if (dev < 64 && !(configured & (1ull << dev))) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
       if (e != cudaSuccess) return e;
       configured |= 1ull << dev;
     }
@@ -968,7 +1069,7 @@ cudaError_t launch_t(const FwdProblem& p, int S, float* part, cudaStream_t strea
   const int sms = device_sms(dev);
   const int grid = static_cast<int>(units < sms ? units : sms);
   const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p.o, p.lse, p.T_q, p.T_kv, BH, n_pairs,
+  kern<<<grid, kThreads, smem_bytes, stream>>>(mq, mk, mv, p.o, p.lse, p.T_q, p.T_kv, BH, n_pairs,
                                                   scale_log2, p.causal, p.status, p.h, p.h_kv, S,
                                                   part, pkv);
   return cudaGetLastError();
@@ -982,9 +1083,7 @@ cudaError_t launch_prefill(const FwdProblem& p, int num_splits, float* part, cud
   const bool split = num_splits > 1;
   const PagedKV none{nullptr, nullptr, 0, 0, 0};
   if (p.d == 64) {
-    // short queries: two heads per unit (head-pair mode); not with a paged
-    // cache, whose one producer thread would then make twice the page-table
-    // lookups per key tile (measured slower)
+    // short queries: two heads per unit (head-pair mode)
     if (head_pair_mode(64, p.T_q, static_cast<long long>(p.B) * p.h))
       e = p.bf16 ? launch_t<64, true, false, true>(p, num_splits, part, stream, none, nullptr, nullptr)
                  : launch_t<64, false, false, true>(p, num_splits, part, stream, none, nullptr, nullptr);
@@ -1017,8 +1116,14 @@ cudaError_t launch_prefill_paged(const FwdProblem& p, const int* table, const in
   const PagedKV pkv{table, lens, page_shift, max_pages, num_pages};
   cudaError_t e;
   if (p.d == 64) {
-    e = p.bf16 ? launch_t<64, true, true, false>(p, num_splits, part, stream, pkv, p.k, p.v)
-               : launch_t<64, false, true, false>(p, num_splits, part, stream, pkv, p.k, p.v);
+    // two heads per unit (head pairs) when the query rows fit one tile and
+    // the pages hold 64 rows or more
+    if (paged_head_pairs(64, p.T_q, static_cast<long long>(p.B) * p.h, 1 << page_shift))
+      e = p.bf16 ? launch_t<64, true, true, true>(p, num_splits, part, stream, pkv, p.k, p.v)
+                 : launch_t<64, false, true, true>(p, num_splits, part, stream, pkv, p.k, p.v);
+    else
+      e = p.bf16 ? launch_t<64, true, true, false>(p, num_splits, part, stream, pkv, p.k, p.v)
+                 : launch_t<64, false, true, false>(p, num_splits, part, stream, pkv, p.k, p.v);
     *name = p.bf16 ? "prefill_paged_tcgen05_d64_bf16+decode_combine"
                    : "prefill_paged_tcgen05_d64_f16+decode_combine";
   } else {

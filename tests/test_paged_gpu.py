@@ -202,6 +202,12 @@ TC_CASES = [
     # different sequences (different lengths), the last unit has one head
     (3, 4, 1, [1000, 7, 517], 64, BF16, 16, 0),
     (3, 4, 1, [300, 0, 50], 64, BF16, 16, 1),       # length 0, one partition: o = 0
+    # the same with 64- and 256-row pages: two heads per unit (head pairs),
+    # each tile's table entries staged in shared memory
+    (3, 4, 1, [1000, 7, 517], 64, BF16, 64, 0),
+    (3, 4, 1, [300, 0, 50], 64, F16, 64, 1),
+    (3, 4, 1, [2500, 130, 1], 64, BF16, 256, 3),
+    (2, 16, 4, [5000, 4999], 64, BF16, 128, 0),     # same sequence in both heads
     (4, 8, 1, [0, 2000, 64, 900], 64, F16, 8, 0),   # length 0 in a unit's first head
     # pages of >= 64 rows at d = 64: two heads per unit, each with its own
     # page lookups (pipelined one key tile ahead)
@@ -221,8 +227,11 @@ def test_paged_decode_tensor_core_path(case):
     compare_paged(o, lse, oracle_paged(q, kp, vp, table, ln), dt, f"paged tc {case}")
 
 
-def test_paged_tensor_core_bad_table_entry_is_reported():
-    q, kp, vp, table, ln = make_paged(2, 8, 2, [300, 200], 64, BF16, 16, seed=47)
+@pytest.mark.parametrize("ps", [16, 64])
+def test_paged_tensor_core_bad_table_entry_is_reported(ps):
+    # 16-row pages: one head per unit, the entry read per box; 64-row pages:
+    # head pairs, the entry read while the unit's entries are staged
+    q, kp, vp, table, ln = make_paged(2, 8, 2, [300, 200], 64, BF16, ps, seed=47)
     bad = table.clone()
     bad[1, 1] = kp.shape[0] + 3
     gpu_paged(q, kp, vp, bad, ln, check_status=False)
