@@ -36,8 +36,12 @@
 //   KV mode (X=K, Y=V, U=Q, W=dO):  dV += P_t^T dO_t,  dK += dS_t^T Q_t
 //   Q mode  (X=Q, Y=dO, U=K, W=V):  dQ += dS_t K_t
 // The scores of tile t+1 go into the other buffer while the elementwise warps
-// work on tile t. TMEM: buffers [0,128) and [128,256) (S then dP, 64 columns
-// each), dV at 256, dK or dQ at 256 + d: 512 columns at d = 128.
+// work on tile t. In KV mode P_t is stored and released first (its own
+// barrier), so dV += P_t^T dO_t runs while the warps form dS_t; Q mode stores
+// only dS_t. The streamed rows' lse and D are read from shared memory before
+// the TMEM loads, so their latency overlaps. TMEM: buffers [0,128) and
+// [128,256) (S then dP, 64 columns each), dV at 256, dK or dQ at 256 + d:
+// 512 columns at d = 128.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -79,8 +83,8 @@ struct BwdCfg {
   static constexpr int OFF_RING = 2 * RES_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * STAGE_BYTES;
   // res_full, stage_full[ST], stage_empty[ST], sp_full[2], p_full[2], acc_full, mma_done,
-  // res_tmem
-  static constexpr int N_BARS = 1 + 2 * STAGES + 7;
+  // res_tmem, p_half[2]
+  static constexpr int N_BARS = 1 + 2 * STAGES + 9;
   static constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* acc_full = p_full + 2;
   uint64_t* mma_done = acc_full + 1;
   uint64_t* res_tmem = mma_done + 1;   // X and Y copied into TMEM (XY_TMEM)
+  uint64_t* p_half = res_tmem + 1;     // KV: P_t stored (dS_t still being formed)
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMPTR);
 
   const int warp = threadIdx.x >> 5;
@@ -284,6 +289,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(mma_done, 1);
     ptx::mbar_init(res_tmem, kEltThreads);
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&p_half[b], kEltThreads);
     ptx::fence_mbarrier_init();
   }
   if (warp == kWarpMma) {
@@ -391,9 +397,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_grads = [&](int b, int slot, bool first) {
+    // dV += P_t^T dO_t (KV only): needs P_t alone
+    auto issue_dv = [&](int b, int slot, bool first) {
       const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
-      const uint64_t u0 = dUm + so, w0 = dWm + so;
+      const uint64_t w0 = dWm + so;
       const uint32_t a0 = tmem + col_buf(b);
       if (ptx::elect_one_sync()) {
 #pragma unroll
@@ -402,7 +409,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
           // streamed rows 16kk..16kk+15: half kk/2, 16-bit pairs from column 8*(kk%2)
           const uint32_t a_col = a0 + (kk >> 1) * 32 + (kk & 1) * 8;
-          if constexpr (KV) ptx::mma_f16_ts(tmem + kColAcc1, a_col, w0 + bo, idG, acc);
+          ptx::mma_f16_ts(tmem + kColAcc1, a_col, w0 + bo, idG, acc);
+        }
+      }
+      __syncwarp();
+    };
+    // dK += dS_t^T Q_t (KV) or dQ += dS_t K_t (Q); frees the stage
+    auto issue_ds = [&](int b, int slot, bool first) {
+      const uint64_t so = static_cast<uint64_t>(slot * C::STAGE_BYTES) >> 4;
+      const uint64_t u0 = dUm + so;
+      const uint32_t a0 = tmem + col_buf(b);
+      if (ptx::elect_one_sync()) {
+#pragma unroll
+        for (int kk = 0; kk < kStr / 16; ++kk) {
+          const uint64_t bo = static_cast<uint64_t>(kk * 16 * 128) >> 4;
+          const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
+          const uint32_t a_col = a0 + (kk >> 1) * 32 + (kk & 1) * 8;
           ptx::mma_f16_ts(tmem + C::COL_ACC2, a_col + 64, u0 + bo, idG, acc);
         }
         ptx::mma_commit(&stage_empty[slot]);
@@ -433,10 +455,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tc_fence_after();
         issue_scores(b ^ 1, s1);
       }
+      if constexpr (KV) {
+        ok = wait(&p_half[b], (it >> 1) & 1, kSiteMmaP);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_dv(b, it % ST, it == 0);
+      }
       ok = wait(&p_full[b], (it >> 1) & 1, kSiteMmaP);
       if (!ok) break;
       ptx::tc_fence_after();
-      issue_grads(b, it % ST, it == 0);
+      issue_ds(b, it % ST, it == 0);
     }
     // every MMA issued must be complete before TMEM is freed
     if (ptx::elect_one_sync()) {
@@ -505,6 +533,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
+      // the streamed rows' lse and D (KV): read before the TMEM loads so
+      // their latency overlaps
+      float4 lv[8], dv4[8];
+      if constexpr (KV) {
+        const float* v0 = reinterpret_cast<const float*>(smem + C::OFF_RING +
+                                                         slot * C::STAGE_BYTES + 2 * C::STR_BYTES);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          lv[c4] = reinterpret_cast<const float4*>(v0 + half * 32)[c4];
+          dv4[c4] = reinterpret_cast<const float4*>(v0 + kStr + half * 32)[c4];
+        }
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          lv[c4] = make_float4(l2_row, l2_row, l2_row, l2_row);
+          dv4[c4] = make_float4(dd_row, dd_row, dd_row, dd_row);
+        }
+      }
       uint32_t sr[64];
       ptx::tmem_ld_32x32b_x32(t_half + col_buf(b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       ptx::tmem_ld_32x32b_x32(t_half + col_buf(b) + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
@@ -526,26 +572,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         cmax = (causal ? min(rrow + off, T_kv - 1) : T_kv - 1) - s0;
       }
       const bool all_visible = __all_sync(0xffffffffu, cmin <= 0 && cmax >= 31);
-      const float4* vl2 = nullptr;
-      const float4* vdd = nullptr;
-      if constexpr (KV) {
-        const float* v0 = reinterpret_cast<const float*>(smem + C::OFF_RING +
-                                                         slot * C::STAGE_BYTES + 2 * C::STR_BYTES);
-        vl2 = reinterpret_cast<const float4*>(v0 + half * 32);
-        vdd = reinterpret_cast<const float4*>(v0 + kStr + half * 32);
-      }
       // three passes without branches inside, so the 32 columns' chains
       // interleave: exponentials, then (diagonal tiles only) the mask, then
       // dS and the 16-bit pairs
       float2 pp[16];
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        float4 l;
-        if constexpr (KV) {
-          l = vl2[c4];
-        } else {
-          l = make_float4(l2_row, l2_row, l2_row, l2_row);
-        }
+        const float4 l = lv[c4];
         const float2 x0 = __ffma2_rn(make_float2(s[4 * c4], s[4 * c4 + 1]), sl2, make_float2(-l.x, -l.y));
         const float2 x1 =
             __ffma2_rn(make_float2(s[4 * c4 + 2], s[4 * c4 + 3]), sl2, make_float2(-l.z, -l.w));
@@ -560,25 +593,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       uint32_t pk[16], gk[16];
+      if constexpr (KV) {
+        // P over the first 16 columns of this warp's half of S, released at
+        // once: dV += P^T dO runs while dS is formed
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(pp[c].x, pp[c].y);
+        ptx::tmem_st_32x32b_x16(t_half + col_buf(b), pk);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&p_half[b]);
+      }
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        float4 dd;
-        if constexpr (KV) {
-          dd = vdd[c4];
-        } else {
-          dd = make_float4(dd_row, dd_row, dd_row, dd_row);
-        }
+        const float4 dd = dv4[c4];
         const float2 g0 = __fmul2_rn(pp[2 * c4], __fadd2_rn(make_float2(dp[4 * c4], dp[4 * c4 + 1]),
                                                              make_float2(-dd.x, -dd.y)));
         const float2 g1 = __fmul2_rn(pp[2 * c4 + 1], __fadd2_rn(make_float2(dp[4 * c4 + 2], dp[4 * c4 + 3]),
                                                                  make_float2(-dd.z, -dd.w)));
-        pk[2 * c4] = pack2<BF16>(pp[2 * c4].x, pp[2 * c4].y);
-        pk[2 * c4 + 1] = pack2<BF16>(pp[2 * c4 + 1].x, pp[2 * c4 + 1].y);
         gk[2 * c4] = pack2<BF16>(g0.x, g0.y);
         gk[2 * c4 + 1] = pack2<BF16>(g1.x, g1.y);
       }
-      // P over the first 16 columns of this warp's half of S, dS likewise in dP
-      ptx::tmem_st_32x32b_x16(t_half + col_buf(b), pk);
+      // dS over the first 16 columns of this warp's half of dP
       ptx::tmem_st_32x32b_x16(t_half + col_buf(b) + 64, gk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();

@@ -40,6 +40,7 @@
 
 #include "attn_internal.h"
 #include "attn_status.h"
+#include "merge_sm103.cuh"
 
 namespace attn {
 
@@ -532,76 +533,14 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(128)
     decode_combine_kernel(const float* __restrict__ ws, uint8_t* __restrict__ out,
                           float* __restrict__ lse, int BH, int S) {
-  constexpr int PER = D / 32;   // dims per lane
   // wait for the split grid (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x * 4 + warp;
   if (bh >= BH) return;
-  const size_t stride = decode_partial_floats(D);
-  const float* part = ws + static_cast<size_t>(bh) * S * stride;
-
-  // each lane reads the (m, l) of partitions lane, lane+32, ... at once
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, part[s * stride + D]);
-#pragma unroll
-  for (int w = 16; w > 0; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
-  // M is finite unless the row has no keys (paged path, length 0)
-  float L = 0.f;
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    const int s_mine = s0 + lane;
-    float w_mine = 0.f;
-    if (s_mine < S) {
-      const float ms = part[s_mine * stride + D];
-      w_mine = (ms == -INFINITY) ? 0.f : ex2f(ms - M);
-      L = fmaf(w_mine, part[s_mine * stride + D + 1], L);
-    }
-    const int n = min(32, S - s0);
-    // weights broadcast from the lane that computed them; the o loads of
-    // different partitions are independent and overlap
-#pragma unroll 8
-    for (int t = 0; t < n; ++t) {
-      const float w = __shfl_sync(0xffffffffu, w_mine, t);
-      const float* ps = part + (s0 + t) * stride + lane * PER;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, ps[i], acc[i]);
-    }
-  }
-#pragma unroll
-  for (int w = 16; w > 0; w >>= 1) L += __shfl_xor_sync(0xffffffffu, L, w);
-  // L = 0 only for a row with no keys at all (a zero-length sequence of the
-  // paged path): output 0 and lse -inf instead of 0/0
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint8_t* orow = out + static_cast<size_t>(bh) * D * 2 + lane * PER * 2;
-  if constexpr (PER == 2) {
-    uint32_t w;
-    if constexpr (BF16) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-      w = *reinterpret_cast<uint32_t*>(&h);
-    } else {
-      __half2 h = __floats2half2_rn(acc[0] * inv, acc[1] * inv);
-      w = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint32_t*>(orow) = w;
-  } else {
-    uint32_t w[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      if constexpr (BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-        w[i] = *reinterpret_cast<uint32_t*>(&h);
-      } else {
-        __half2 h = __floats2half2_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-        w[i] = *reinterpret_cast<uint32_t*>(&h);
-      }
-    }
-    *reinterpret_cast<uint2*>(orow) = make_uint2(w[0], w[1]);
-  }
-  if (lane == 0) lse[bh] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+  merge::merge_row<D, BF16>(ws + static_cast<size_t>(bh) * S * decode_partial_floats(D), S,
+                            out + static_cast<size_t>(bh) * D * 2, lse + bh, lane);
 }
 
 template <int D, bool BF16, int G>

@@ -6,7 +6,8 @@ kernel combines per query row.
 Cases: short queries against a long causal context (the chunked-prefill
 shape), non-causal, ragged query and key tails, more partitions than key
 tiles (empty partitions), grouped-query heads, d = 64 and 128, bf16 and
-fp16, automatic and fixed partition counts, caller and library workspace."""
+fp16, automatic and fixed partition counts, caller and library workspace,
+more units than SMs, and a caller workspace holding stale bytes."""
 
 import numpy as np
 import pytest
@@ -49,6 +50,8 @@ CASES = [
     (1, 3, 1, 2, 1000, 128, BF16, True, 4),        # two query rows
     (1, 1, 1, 512, 512, 64, F16, True, 3),         # causal square: early pairs see few tiles
     (1, 2, 2, 200, 8192, 128, BF16, False, 64),    # the most partitions
+    (1, 8, 8, 1024, 2048, 128, BF16, True, 8),     # more units than SMs: CTAs loop, then merge
+    (1, 6, 6, 100, 5000, 64, F16, False, 16),      # head pairs (d 64, one query tile)
 ]
 
 
@@ -94,3 +97,17 @@ def test_splitkv_one_partition_is_the_plain_kernel():
     o, lse = gpu_splitkv(q, k, v, True, 1)
     assert _lib.last_kernel_name() == "prefill_tcgen05_d64_bf16"
     compare(o, lse, oracle_fwd(q, k, v, True), BF16, "splitkv S=1")
+
+
+def test_splitkv_ignores_stale_workspace_bytes():
+    """A caller workspace filled with 0xff bytes, then the same workspace
+    reused, give the oracle's result with the same bits: nothing the call
+    reads from the workspace comes from an earlier call."""
+    q, k, v = make_qkv(1, 4, 256, 6000, 64, BF16, seed=55)
+    nbytes = _lib.splitkv_workspace_bytes(1, 4, 256, 6000, 64, 9)
+    ws = torch.full((nbytes,), 255, dtype=torch.uint8, device="cuda")
+    a = gpu_splitkv(q, k, v, True, 9, workspace=ws)
+    assert _lib.last_kernel_name() == "prefill_splitkv_tcgen05_d64_bf16+decode_combine"
+    compare(a[0], a[1], oracle_fwd(q, k, v, True), BF16, "split-KV, stale workspace")
+    b = gpu_splitkv(q, k, v, True, 9, workspace=ws)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
