@@ -49,11 +49,12 @@ METRIC = "causal prefill attention TFLOP/s + decode KV GB/s, as % of GB300 roofl
 UNIT = "% of one GB300 roofline (whole job)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+_CSRC = os.path.join(ROOT, "exact_io_aware_attn_gb300", "csrc")
+# the sources each traffic entry's kernels are built from
 KERNEL_SOURCES = {
-    "decode": os.path.join(ROOT, "exact_io_aware_attn_gb300", "csrc", "decode_sm103.cu"),
-    "prefill": os.path.join(ROOT, "exact_io_aware_attn_gb300", "csrc", "prefill_sm103.cu"),
-    "prefill_very_long": os.path.join(ROOT, "exact_io_aware_attn_gb300", "csrc",
-                                      "prefill_sm103.cu"),
+    "decode": [os.path.join(_CSRC, "decode_sm103.cu"), os.path.join(_CSRC, "merge_sm103.cuh")],
+    "prefill": [os.path.join(_CSRC, "prefill_sm103.cu")],
+    "prefill_very_long": [os.path.join(_CSRC, "prefill_sm103.cu")],
 }
 # repeats of the step after the timed K steps: >= 3 repeats of >= 20 steps
 REPEATS = 3
@@ -74,9 +75,12 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def source_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic(kind):
