@@ -81,3 +81,31 @@ def test_host_entry_asynchronous_on_a_stream():
     compare(o.double().numpy(), lse.double().numpy(), oracle_fwd(q, k, v, True), BF16,
             "host entry, side stream")
     assert not np.isnan(o.double().numpy()).any()
+
+
+LARGE_CASES = [
+    # B, h_q, h_kv, T_q, T_kv, d, dtype, causal: large inputs, enqueued on a
+    # side stream
+    (4, 8, 8, 1, 16384, 128, BF16, False),    # decode, 256 MiB in
+    (1, 8, 2, 64, 33000, 128, F16, True),     # grouped-query prefill, ~32 MiB in
+]
+
+
+@pytest.mark.parametrize("case", LARGE_CASES, ids=lambda c: "x".join(str(int(x)) for x in c))
+def test_host_entry_large_inputs(case):
+    """Large pinned inputs on a side stream, nothing synchronised before that
+    stream is: the result matches the oracle and, bit for bit, the
+    device-pointer path."""
+    B, hq, hkv, tq, tk, d, dt, causal = case
+    q, k, v = (t.pin_memory() for t in make_qkv(B, hq, tq, tk, d, dt, seed=74, h_kv=hkv))
+    s = torch.cuda.Stream()
+    o = torch.full(q.shape, float("nan"), dtype=q.dtype).pin_memory()
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32).pin_memory()
+    _lib.attn_fwd_host(q, k, v, causal=causal, out=o, lse=lse, stream=s, synchronize=False)
+    s.synchronize()
+    st, word = _lib.get_device_error()
+    assert st == _lib.ATTN_OK, f"device status {st} word {word:#x}"
+    ref = oracle_fwd(q, k, v, causal) if hq == hkv else oracle_fwd_gqa(q, k, v, causal)
+    compare(o.double().numpy(), lse.double().numpy(), ref, dt, f"host entry large {case}")
+    o_dev, lse_dev = _device_ref(q, k, v, causal)
+    assert torch.equal(o, o_dev) and torch.equal(lse, lse_dev)
