@@ -15,14 +15,17 @@
 //   bwd_prep     one pass over O and dO: D and lse * log2(e) per query row,
 //                into a workspace padded to 128 rows per head
 //   bwd (KV)     one CTA per (key/value head, 128-key tile): K and V stay in
-//                shared memory, the CTA streams 64-row tiles of Q and dO
-//                (every query head of the group, causal: only rows that see
-//                the tile) and accumulates dV and dK in tensor memory
+//                shared memory, the CTA streams tiles of Q and dO (every
+//                query head of the group, causal: only rows that see the
+//                tile) and accumulates dV and dK in tensor memory. At d = 64
+//                the streamed 128-row tiles sit on the TMEM lanes
+//                (bwd_kvq_kernel, below); at d = 128 the keys do (bwd_kernel
+//                in KV mode, 64-row streamed tiles)
 //   bwd (Q)      one CTA per (query head, 128-row tile): Q and dO stay, the
 //                CTA streams 64-key tiles of K and V (causal: up to the
 //                diagonal) and accumulates dQ in tensor memory
 //
-// Both modes are one kernel template. Roles (320 threads): warps 0-7 turn
+// bwd_kernel's two modes are one template. Roles (320 threads): warps 0-7 turn
 // scores into P and dS -- warp w owns TMEM lanes 32*(w%4).. (one resident row
 // per thread) and columns 32*(w/4).. of each 64-column score tile, so every
 // sub-partition runs two of them; warp 8 is the TMA producer; warp 9 owns TMEM
@@ -107,7 +110,7 @@ __host__ __device__ constexpr uint32_t col_buf(int b) { return static_cast<uint3
 
 enum : uint32_t {
   kSiteProdStage = 1, kSiteMmaRes, kSiteMmaStage, kSiteMmaP, kSiteEltS, kSiteEltStage, kSiteEltAcc,
-  kSiteEltRes
+  kSiteEltRes, kSiteMmaSFree
 };
 
 template <bool BF16>
@@ -666,6 +669,402 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// dK/dV at d = 64 with the streamed queries on the TMEM lanes. One CTA per
+// (key/value head, 128-key tile): K and V stay in shared memory and the CTA
+// streams 128-row tiles of Q and dO (with their lse*log2(e) and D) through a
+// 3-stage ring, for every query head of the group and, causally, only tiles
+// with a row that sees the key tile. Per tile t the tensor core computes
+//   S_t = Q_t K^T and dP_t = dO_t V^T   (M = 128 query rows, N = 128 keys, K = 64)
+// into TMEM (S in two buffers, dP in one). Elementwise thread (warp w, lane i)
+// owns query row 32*(w%4)+i -- its lse and D are two registers -- and the 64
+// keys 64*(w/4)..: it loads its S and dP values at once (releasing both TMEM
+// buffers for the next products), forms P = 2^(scale*log2e*S - lse*log2e)
+// and dS = P * (dP - D) 32 keys at a time and writes each half as soon as it
+// is formed, as 16-bit rows (one 128-byte row per query and key half,
+// 128-byte swizzle) into shared memory. The tensor core
+// then accumulates dV += P_t^T dO_t and dK += dS_t^T Q_t (M = 128 keys,
+// N = 64, K = 128 queries) with A read MN-major from those rows and B the
+// streamed tile read MN-major. TMEM: S [0,256), dP [256,384), dV [384,448),
+// dK [448,512).
+// ---------------------------------------------------------------------------
+namespace kvq {
+constexpr int kRows = 128;                      // keys per CTA; queries per streamed tile
+constexpr int kTile = kRows * 64 * 2;           // one [128 rows][64] 16-bit tile (128-byte rows)
+constexpr int kStages = 3;
+constexpr int kStageBytes = 2 * kTile + 1024;   // Q, dO, then lse*log2e [128] and D [128]
+constexpr int OFF_K = 0;
+constexpr int OFF_V = kTile;
+constexpr int OFF_RING = 2 * kTile;
+constexpr int OFF_P = OFF_RING + kStages * kStageBytes;  // [key half][128 query rows][128 B]
+constexpr int OFF_DS = OFF_P + 2 * kTile;
+constexpr int OFF_BAR = OFF_DS + 2 * kTile;
+// res_full, stage_full[3], stage_empty[3], s_full[2], s_free[2], dp_full, dp_free, p_ready,
+// pd_free, acc_full, mma_done
+constexpr int N_BARS = 1 + 2 * kStages + 2 + 2 + 6;
+constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
+constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
+constexpr uint32_t COL_S = 0, COL_DP = 256, COL_DV = 384, COL_DK = 448;
+static_assert(kStageBytes % 1024 == 0 && OFF_P % 1024 == 0 && OFF_DS % 1024 == 0, "atoms");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+
+// Unit u (heaviest first under a causal mask: key tile 0 sees every query):
+// the key/value head and 128-key tile, and the streamed 128-row query tiles.
+struct Unit {
+  int res_bh, r0, str_bh0, t_first, per_head, n;
+};
+__device__ __forceinline__ Unit unit_of(int u, int BH_kv, int T_q, int T_kv, int causal, int h,
+                                        int h_kv) {
+  const int group = h / h_kv;
+  const int off = T_kv - T_q;
+  Unit w;
+  w.res_bh = u % BH_kv;
+  w.r0 = (u / BH_kv) * kRows;
+  const int b = w.res_bh / h_kv, kvh = w.res_bh % h_kv;
+  w.str_bh0 = b * h + kvh * group;
+  const int first_row = causal ? max(0, w.r0 - off) : 0;  // key r0 is seen by rows >= r0 - off
+  w.t_first = first_row / kRows;
+  w.per_head = (T_q + kRows - 1) / kRows - w.t_first;
+  w.n = max(0, w.per_head) * group;
+  return w;
+}
+__device__ __forceinline__ void item_of(const Unit& w, int it, int* bh, int* s0) {
+  const int g = it / w.per_head;
+  *bh = w.str_bh0 + g;
+  *s0 = (w.t_first + (it - g * w.per_head)) * kRows;
+}
+}  // namespace kvq
+
+template <bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_kvq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                   const float* __restrict__ ws_l2, const float* __restrict__ ws_dd, int Tq_pad,
+                   void* __restrict__ dv_out, void* __restrict__ dk_out, int T_q, int T_kv,
+                   int BH_kv, int h, int h_kv, float scale, float scale_log2, int causal,
+                   unsigned int* __restrict__ status) {
+  using namespace kvq;
+  constexpr int ST = kStages;
+  constexpr uint32_t kKern = kKernBwdKV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* stage_full = bars + 1;
+  uint64_t* stage_empty = stage_full + ST;
+  uint64_t* s_full = stage_empty + ST;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* dp_full = s_free + 2;
+  uint64_t* dp_free = dp_full + 1;
+  uint64_t* p_ready = dp_free + 1;
+  uint64_t* pd_free = p_ready + 1;
+  uint64_t* acc_full = pd_free + 1;
+  uint64_t* mma_done = acc_full + 1;
+  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Unit w = unit_of(static_cast<int>(blockIdx.x), BH_kv, T_q, T_kv, causal, h, h_kv);
+  const int n = w.n;
+  const int off = T_kv - T_q;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(res_full, 1);
+    for (int i = 0; i < ST; ++i) {
+      ptx::mbar_init(&stage_full[i], 1);
+      ptx::mbar_init(&stage_empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      ptx::mbar_init(&s_free[b], kEltThreads);
+    }
+    ptx::mbar_init(dp_full, 1);
+    ptx::mbar_init(dp_free, kEltThreads);
+    ptx::mbar_init(p_ready, kEltThreads);
+    ptx::mbar_init(pd_free, 1);
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(mma_done, 1);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == kWarpMma) {
+    ptx::tmem_alloc(tmem_ptr, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == kWarpProd) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmK);
+      ptx::prefetch_tensormap(&tmV);
+      ptx::prefetch_tensormap(&tmQ);
+      ptx::prefetch_tensormap(&tmO);
+      const uint64_t pol_str = ptx::policy_evict_last();
+      const uint64_t pol_res = ptx::policy_evict_first();
+      ptx::mbar_arrive_expect_tx(res_full, 2 * kTile);
+      ptx::tma_load_3d(smem + OFF_K, &tmK, res_full, 0, w.r0, w.res_bh, pol_res);
+      ptx::tma_load_3d(smem + OFF_V, &tmV, res_full, 0, w.r0, w.res_bh, pol_res);
+      bool ok = true;
+      int it = 0;
+      for (; it < n; ++it) {
+        const int slot = it % ST;
+        ok = ptx::mbar_wait(&stage_empty[slot], ((it / ST) & 1) ^ 1, status,
+                            status_word(kKern, kSiteProdStage));
+        if (!ok) break;
+        int sbh, s0;
+        item_of(w, it, &sbh, &s0);
+        uint8_t* stg = smem + OFF_RING + slot * kStageBytes;
+        ptx::mbar_arrive_expect_tx(&stage_full[slot], 2 * kTile + 2 * kRows * 4);
+        ptx::tma_load_3d(stg, &tmQ, &stage_full[slot], 0, s0, sbh, pol_str);
+        ptx::tma_load_3d(stg + kTile, &tmO, &stage_full[slot], 0, s0, sbh, pol_str);
+        const size_t vo = static_cast<size_t>(sbh) * Tq_pad + s0;
+        ptx::bulk_load(stg + 2 * kTile, ws_l2 + vo, kRows * 4, &stage_full[slot]);
+        ptx::bulk_load(stg + 2 * kTile + kRows * 4, ws_dd + vo, kRows * 4, &stage_full[slot]);
+      }
+      if (!ok) {
+        // let the copies in flight land before the CTA's shared memory goes
+        mbar_drain(res_full, 0);
+        for (int i = (it > ST ? it - ST : 0); i < it; ++i) mbar_drain(&stage_full[i % ST], (i / ST) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kRows, kRows, false, false);
+    constexpr uint32_t idG = ptx::make_idesc_f16(BF16, kRows, 64, true, true);
+    const uint32_t sK = ptx::smem_u32(smem + OFF_K);
+    const uint32_t sV = ptx::smem_u32(smem + OFF_V);
+    const uint32_t sR = ptx::smem_u32(smem + OFF_RING);
+    const uint64_t dK = ptx::make_sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV = ptx::make_sdesc_sw128(sV, 16, 1024);
+    const uint64_t dPm = ptx::make_sdesc_sw128(ptx::smem_u32(smem + OFF_P), kTile, 1024);
+    const uint64_t dSm = ptx::make_sdesc_sw128(ptx::smem_u32(smem + OFF_DS), kTile, 1024);
+    auto stage_desc = [&](int slot, int which, bool mn) {
+      return ptx::make_sdesc_sw128(sR + slot * kStageBytes + which * kTile, mn ? kTile : 16, 1024);
+    };
+    auto issue_s = [&](int b, int slot) {
+      const uint64_t a0 = stage_desc(slot, 0, false);
+      if (ptx::elect_one_sync()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_f16_ss(tmem + COL_S + b * 128, a0 + kk * 2, dK + kk * 2, idS, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(&s_full[b]);
+      }
+      __syncwarp();
+    };
+    auto issue_dp = [&](int slot) {
+      const uint64_t a0 = stage_desc(slot, 1, false);
+      if (ptx::elect_one_sync()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_f16_ss(tmem + COL_DP, a0 + kk * 2, dV + kk * 2, idS, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(dp_full);
+      }
+      __syncwarp();
+    };
+    auto issue_grads = [&](int slot, bool first) {
+      const uint64_t bq = stage_desc(slot, 0, true);
+      const uint64_t bo = stage_desc(slot, 1, true);
+      if (ptx::elect_one_sync()) {
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk) {
+          const uint64_t step = static_cast<uint64_t>(kk * 16 * 128) >> 4;  // 16 query rows
+          const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
+          ptx::mma_f16_ss(tmem + COL_DV, dPm + step, bo + step, idG, acc);
+          ptx::mma_f16_ss(tmem + COL_DK, dSm + step, bq + step, idG, acc);
+        }
+        ptx::mma_commit(pd_free);
+        ptx::mma_commit(&stage_empty[slot]);
+      }
+      __syncwarp();
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      const bool good = ptx::mbar_wait(bar, parity, status, status_word(kKern, site));
+      return __all_sync(0xffffffffu, good);
+    };
+
+    bool ok = wait(res_full, 0, kSiteMmaRes);
+    for (int i = 0; ok && i < 2 && i < n; ++i) {
+      ok = wait(&stage_full[i], 0, kSiteMmaStage);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_s(i, i);
+      if (i == 0) issue_dp(0);
+    }
+    for (int it = 0; ok && it < n; ++it) {
+      if (it + 1 < n) {
+        // dP of the next tile once the warps have loaded this tile's dP (its
+        // stage was waited for with its scores)
+        ok = wait(dp_free, it & 1, kSiteMmaSFree);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_dp((it + 1) % ST);
+      }
+      ok = wait(p_ready, it & 1, kSiteMmaP);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_grads(it % ST, it == 0);
+      if (it + 2 < n) {
+        const int b = it & 1;
+        ok = wait(&s_free[b], (it >> 1) & 1, kSiteMmaSFree);
+        if (!ok) break;
+        const int s2 = (it + 2) % ST;
+        ok = wait(&stage_full[s2], ((it + 2) / ST) & 1, kSiteMmaStage);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_s(b, s2);
+      }
+    }
+    // every MMA issued must be complete before TMEM is freed
+    if (ptx::elect_one_sync()) {
+      if (ok) ptx::mma_commit(acc_full);
+      ptx::mma_commit(mma_done);
+    }
+    __syncwarp();
+    mbar_drain(mma_done, 0);
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    const int quarter = warp & 3;                    // TMEM lanes 32*quarter..
+    const int half = warp >> 2;                      // keys 64*half.. of the tile
+    const int row = quarter * 32 + lane;             // query row of a streamed tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
+    const int k0 = w.r0 + half * 64;                 // first key of this thread's 64
+    bool ok = true;
+    for (int it = 0; ok && it < n; ++it) {
+      const int b = it & 1;
+      const int slot = it % ST;
+      ok = ptx::mbar_wait(&s_full[b], (it >> 1) & 1, status, status_word(kKern, kSiteEltS));
+      if (ok) ok = ptx::mbar_wait(dp_full, it & 1, status, status_word(kKern, kSiteEltS));
+      if (ok)
+        ok = ptx::mbar_wait(&stage_full[slot], (it / ST) & 1, status,
+                            status_word(kKern, kSiteEltStage));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      int sbh, s0;
+      item_of(w, it, &sbh, &s0);
+      const uint8_t* stg = smem + OFF_RING + slot * kStageBytes;
+      const float l2 = reinterpret_cast<const float*>(stg + 2 * kTile)[row];
+      const float dd = reinterpret_cast<const float*>(stg + 2 * kTile + kRows * 4)[row];
+      const float2 nl = make_float2(-l2, -l2);
+      const float2 nd = make_float2(-dd, -dd);
+      // keys k0 + c visible: c <= cmax (causal, and keys past T_kv)
+      const int q = s0 + row;
+      const int cmax = min(T_kv - 1, causal ? q + off : T_kv - 1) - k0;
+      const bool all_visible = __all_sync(0xffffffffu, cmax >= 63);
+      // S and dP of the thread's 64 keys, all loaded before any use; the
+      // buffers are released at once (the next products may overwrite them)
+      uint32_t sr[128];
+      ptx::tmem_ld_32x32b_x32(t_lane + COL_S + b * 128 + half * 64,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      ptx::tmem_ld_32x32b_x32(t_lane + COL_DP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      ptx::tmem_ld_32x32b_x32(t_lane + COL_S + b * 128 + half * 64 + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+      ptx::tmem_ld_32x32b_x32(t_lane + COL_DP + half * 64 + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+      tmem_wait_ld_64(*reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
+      tmem_wait_ld_64(*reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&s_free[b]);
+      ptx::mbar_arrive(dp_free);
+      uint8_t* prow = smem + OFF_P + half * kTile + row * 128;
+      uint8_t* grow = smem + OFF_DS + half * kTile + row * 128;
+#pragma unroll
+      for (int c32 = 0; c32 < 2; ++c32) {
+        const float* s = reinterpret_cast<const float*>(sr + c32 * 64);
+        const float* dp = reinterpret_cast<const float*>(sr + c32 * 64 + 32);
+        float2 pp[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 x = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), sl2, nl);
+          pp[j] = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+        }
+        if (!all_visible) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = c32 * 32 + 2 * j;
+            pp[j].x = c <= cmax ? pp[j].x : 0.f;
+            pp[j].y = c + 1 <= cmax ? pp[j].y : 0.f;
+          }
+        }
+        uint32_t pk[16], gk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 g = __fmul2_rn(pp[j], __fadd2_rn(make_float2(dp[2 * j], dp[2 * j + 1]), nd));
+          pk[j] = pack2<BF16>(pp[j].x, pp[j].y);
+          gk[j] = pack2<BF16>(g.x, g.y);
+        }
+        if (c32 == 0 && it >= 1) {
+          // the previous tile's gradient products read the P and dS rows
+          bool good = ptx::mbar_wait(pd_free, (it - 1) & 1, status, status_word(kKern, kSiteEltStage));
+          good = __all_sync(0xffffffffu, good);
+          if (!good) {
+            ok = false;
+            break;
+          }
+        }
+        // this half's 32 keys of the query's P and dS rows: chunks 4*c32 ..
+        // 4*c32+3 of 16 bytes, chunk c at position c ^ (row % 8)
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int pos = ((c32 * 4 + c4) ^ (row & 7)) << 4;
+          *reinterpret_cast<uint4*>(prow + pos) =
+              make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+          *reinterpret_cast<uint4*>(grow + pos) =
+              make_uint4(gk[4 * c4], gk[4 * c4 + 1], gk[4 * c4 + 2], gk[4 * c4 + 3]);
+        }
+      }
+      if (!ok) break;
+      // generic-proxy writes, read next by the tensor core
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(p_ready);
+    }
+    if (ok) {
+      // -------------------------------------------------------------- epilogue
+      ok = ptx::mbar_wait(acc_full, 0, status, status_word(kKern, kSiteEltAcc));
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        ptx::tc_fence_after();
+        const int key = w.r0 + row;  // accumulator lanes are keys
+        const bool write = key < T_kv;
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          uint8_t* dst = reinterpret_cast<uint8_t*>(a == 0 ? dv_out : dk_out) +
+                         (static_cast<size_t>(w.res_bh) * T_kv + (write ? key : 0)) * 64 * 2 +
+                         half * 32 * 2;
+          const float mul = a == 0 ? 1.f : scale;
+          uint32_t raw[32];
+          ptx::tmem_ld_32x32b_x32(t_lane + (a == 0 ? COL_DV : COL_DK) + half * 32, raw);
+          tmem_wait_ld_32(raw);
+          if (write) {
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+              const float* f = reinterpret_cast<const float*>(&raw[g8 * 8]);
+              uint4 v;
+              v.x = pack2<BF16>(f[0] * mul, f[1] * mul);
+              v.y = pack2<BF16>(f[2] * mul, f[3] * mul);
+              v.z = pack2<BF16>(f[4] * mul, f[5] * mul);
+              v.w = pack2<BF16>(f[6] * mul, f[7] * mul);
+              *reinterpret_cast<uint4*>(dst + g8 * 16) = v;
+            }
+          }
+        }
+      }
+    }
+    ptx::tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == kWarpMma) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
 template <typename K>
 cudaError_t configure_once(K kern, int smem_bytes, uint64_t* configured, int dev) {
   if (dev >= 64 || (*configured & (1ull << dev))) return cudaSuccess;
@@ -709,6 +1108,25 @@ cudaError_t launch_bwd_t(const BwdProblem& p, cudaStream_t stream) {
 
   // 2. dK, dV: resident K/V tiles, streamed Q/dO tiles
   CUtensorMap mX, mY, mU, mW;
+  if constexpr (D == 64) {
+    // the streamed queries on the TMEM lanes (bwd_kvq_kernel)
+    auto kern_kvq = bwd_kvq_kernel<BF16>;
+    static uint64_t conf_kvq = 0;
+    {
+      std::lock_guard<std::mutex> g(mu);
+      e = configure_once(kern_kvq, kvq::SMEM_BYTES, &conf_kvq, dev);
+      if (e != cudaSuccess) return e;
+    }
+    if (!make_map(&mX, p.k, p.T_kv, BH_kv, D, BF16, kvq::kRows) ||
+        !make_map(&mY, p.v, p.T_kv, BH_kv, D, BF16, kvq::kRows) ||
+        !make_map(&mU, p.q, p.T_q, BH, D, BF16, kvq::kRows) ||
+        !make_map(&mW, p.dout, p.T_q, BH, D, BF16, kvq::kRows))
+      return cudaErrorInvalidValue;
+    const int n_kt = (p.T_kv + kvq::kRows - 1) / kvq::kRows;
+    kern_kvq<<<static_cast<unsigned>(BH_kv) * n_kt, kBwdThreads, kvq::SMEM_BYTES, stream>>>(
+        mX, mY, mU, mW, l2, dd, Tq_pad, p.dv, p.dk, p.T_q, p.T_kv, BH_kv, p.h, p.h_kv, p.scale,
+        scale_log2, p.causal, p.status);
+  } else {
   if (!make_map(&mX, p.k, p.T_kv, BH_kv, D, BF16, kRes) ||
       !make_map(&mY, p.v, p.T_kv, BH_kv, D, BF16, kRes) ||
       !make_map(&mU, p.q, p.T_q, BH, D, BF16, kStr) ||
@@ -718,6 +1136,7 @@ cudaError_t launch_bwd_t(const BwdProblem& p, cudaStream_t stream) {
   kern_kv<<<static_cast<unsigned>(BH_kv) * n_kt, kBwdThreads, CK::SMEM_BYTES, stream>>>(
       mX, mY, mU, mW, l2, dd, Tq_pad, p.dv, p.dk, p.T_q, p.T_kv, BH_kv, n_kt, p.h, p.h_kv, p.scale,
       scale_log2, p.causal, p.status);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
