@@ -18,12 +18,16 @@
 //                shared memory, the CTA streams tiles of Q and dO (every
 //                query head of the group, causal: only rows that see the
 //                tile) and accumulates dV and dK in tensor memory. At d = 64
-//                the streamed 128-row tiles sit on the TMEM lanes
-//                (bwd_kvq_kernel, below); at d = 128 the keys do (bwd_kernel
-//                in KV mode, 64-row streamed tiles)
+//                the streamed tiles have 128 rows (bwd_kv128_kernel,
+//                below); at d = 128 they have 64 (bwd_kernel in KV mode)
 //   bwd (Q)      one CTA per (query head, 128-row tile): Q and dO stay, the
-//                CTA streams 64-key tiles of K and V (causal: up to the
-//                diagonal) and accumulates dQ in tensor memory
+//                CTA streams tiles of K and V (causal: up to the diagonal)
+//                and accumulates dQ in tensor memory. At d = 64 the streamed
+//                tiles have 128 keys (bwd_q128_kernel, below); at d = 128
+//                they have 64 (bwd_kernel in Q mode)
+//
+// All three gradient kernels share the roles (320 threads): warps 0-7 form P
+// and dS, warp 8 is the TMA producer, warp 9 owns TMEM and issues the MMAs.
 //
 // bwd_kernel's two modes are one template. Roles (320 threads): warps 0-7 turn
 // scores into P and dS -- warp w owns TMEM lanes 32*(w%4).. (one resident row
@@ -99,9 +103,7 @@ struct BwdCfg {
   static constexpr uint32_t COL_X = KV ? 256u + 2u * D : 256u;  // Q mode: the unused dV columns
   static constexpr uint32_t COL_Y = COL_X + D / 2;
 };
-static_assert(BwdCfg<64, true>::COL_Y + 32 <= 512, "tensor memory");
 static_assert(BwdCfg<128, false>::COL_Y + 64 <= BwdCfg<128, false>::COL_ACC2, "tensor memory");
-static_assert(BwdCfg<64, false>::COL_Y + 32 <= BwdCfg<64, false>::COL_ACC2, "tensor memory");
 static_assert(BwdCfg<128, true>::SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(BwdCfg<128, false>::SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(BwdCfg<128, true>::COL_ACC2 + 128 <= 512, "tensor memory");
@@ -670,42 +672,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dK/dV at d = 64 with the streamed queries on the TMEM lanes. One CTA per
-// (key/value head, 128-key tile): K and V stay in shared memory and the CTA
-// streams 128-row tiles of Q and dO (with their lse*log2(e) and D) through a
-// 3-stage ring, for every query head of the group and, causally, only tiles
-// with a row that sees the key tile. Per tile t the tensor core computes
-//   S_t = Q_t K^T and dP_t = dO_t V^T   (M = 128 query rows, N = 128 keys, K = 64)
-// into TMEM (S in two buffers, dP in one). Elementwise thread (warp w, lane i)
-// owns query row 32*(w%4)+i -- its lse and D are two registers -- and the 64
-// keys 64*(w/4)..: it loads its S and dP values at once (releasing both TMEM
-// buffers for the next products), forms P = 2^(scale*log2e*S - lse*log2e)
-// and dS = P * (dP - D) 32 keys at a time and writes each half as soon as it
-// is formed, as 16-bit rows (one 128-byte row per query and key half,
-// 128-byte swizzle) into shared memory. The tensor core
-// then accumulates dV += P_t^T dO_t and dK += dS_t^T Q_t (M = 128 keys,
-// N = 64, K = 128 queries) with A read MN-major from those rows and B the
-// streamed tile read MN-major. TMEM: S [0,256), dP [256,384), dV [384,448),
-// dK [448,512).
+// dK/dV at d = 64 with 128-row streamed query tiles. One CTA per (key/value
+// head, 128-key tile): K and V stay in shared memory and the CTA streams
+// 128-row tiles of Q and dO (with their lse*log2(e) and D) through a 5-stage
+// ring, for every query head of the group and, causally, only tiles with a
+// row that sees the key tile. The keys sit on the TMEM lanes. Per tile t the
+// tensor core computes
+//   S_t^T = K Q_t^T and dP_t^T = V dO_t^T   (M = 128 keys, N = 128 queries, K = 64)
+// from shared memory into TMEM (S in two buffers, dP in one). Elementwise
+// thread (warp w, lane i) owns key 32*(w%4)+i and the 64 queries 64*(w/4)..
+// of each tile, whose lse and D it reads from the stage as broadcasts. It
+// forms P = 2^(scale*log2e*S - lse*log2e) and stores it as 16-bit pairs over
+// the first 32 of its 64 S columns; once dP is there it forms
+// dS = P * (dP - D) and stores it the same way over its dP columns. The
+// tensor core accumulates dV += P_t^T dO_t and dK += dS_t^T Q_t (M = 128
+// keys, N = 64, K = 128 queries) with A read from TMEM and B the streamed
+// tile read MN-major, so shared memory carries only the four products' B
+// operands and the score products' A. Issue order dV(t), dK(t), dP(t+1),
+// S(t+2): every product overwrites a buffer only after the products that
+// read it (one thread's MMAs execute in order), and the warps form P(t+1)
+// while dK(t) and dP(t+1) run, dS(t+1) while dV(t+1) and S(t+2) run. P's
+// barrier alternates between two, so that none can complete a second phase
+// before the issuer has waited for the first: P(t+2) needs S(t+2), issued
+// only after the wait for P(t).
+// TMEM: S [0,256), dP [256,384), dV [384,448), dK [448,512).
 // ---------------------------------------------------------------------------
-namespace kvq {
+namespace kv128 {
 constexpr int kRows = 128;                      // keys per CTA; queries per streamed tile
 constexpr int kTile = kRows * 64 * 2;           // one [128 rows][64] 16-bit tile (128-byte rows)
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kStageBytes = 2 * kTile + 1024;   // Q, dO, then lse*log2e [128] and D [128]
 constexpr int OFF_K = 0;
 constexpr int OFF_V = kTile;
 constexpr int OFF_RING = 2 * kTile;
-constexpr int OFF_P = OFF_RING + kStages * kStageBytes;  // [key half][128 query rows][128 B]
-constexpr int OFF_DS = OFF_P + 2 * kTile;
-constexpr int OFF_BAR = OFF_DS + 2 * kTile;
-// res_full, stage_full[3], stage_empty[3], s_full[2], s_free[2], dp_full, dp_free, p_ready,
-// pd_free, acc_full, mma_done
-constexpr int N_BARS = 1 + 2 * kStages + 2 + 2 + 6;
+constexpr int OFF_BAR = OFF_RING + kStages * kStageBytes;
+// res_full, stage_full[5], stage_empty[5], s_full[2], dp_full, p_ready[2], ds_ready, acc_full,
+// mma_done
+constexpr int N_BARS = 1 + 2 * kStages + 2 + 6;
 constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
 constexpr uint32_t COL_S = 0, COL_DP = 256, COL_DV = 384, COL_DK = 448;
-static_assert(kStageBytes % 1024 == 0 && OFF_P % 1024 == 0 && OFF_DS % 1024 == 0, "atoms");
+static_assert(kStageBytes % 1024 == 0 && OFF_RING % 1024 == 0, "atoms");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // Unit u (heaviest first under a causal mask: key tile 0 sees every query):
@@ -733,17 +740,17 @@ __device__ __forceinline__ void item_of(const Unit& w, int it, int* bh, int* s0)
   *bh = w.str_bh0 + g;
   *s0 = (w.t_first + (it - g * w.per_head)) * kRows;
 }
-}  // namespace kvq
+}  // namespace kv128
 
 template <bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_kvq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
-                   const float* __restrict__ ws_l2, const float* __restrict__ ws_dd, int Tq_pad,
-                   void* __restrict__ dv_out, void* __restrict__ dk_out, int T_q, int T_kv,
-                   int BH_kv, int h, int h_kv, float scale, float scale_log2, int causal,
-                   unsigned int* __restrict__ status) {
-  using namespace kvq;
+    bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                     const float* __restrict__ ws_l2, const float* __restrict__ ws_dd, int Tq_pad,
+                     void* __restrict__ dv_out, void* __restrict__ dk_out, int T_q, int T_kv,
+                     int BH_kv, int h, int h_kv, float scale, float scale_log2, int causal,
+                     unsigned int* __restrict__ status) {
+  using namespace kv128;
   constexpr int ST = kStages;
   constexpr uint32_t kKern = kKernBwdKV;
   extern __shared__ uint8_t smem_raw[];
@@ -754,12 +761,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* stage_full = bars + 1;
   uint64_t* stage_empty = stage_full + ST;
   uint64_t* s_full = stage_empty + ST;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* dp_full = s_free + 2;
-  uint64_t* dp_free = dp_full + 1;
-  uint64_t* p_ready = dp_free + 1;
-  uint64_t* pd_free = p_ready + 1;
-  uint64_t* acc_full = pd_free + 1;
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* p_ready = dp_full + 1;  // [2]
+  uint64_t* ds_ready = p_ready + 2;
+  uint64_t* acc_full = ds_ready + 1;
   uint64_t* mma_done = acc_full + 1;
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
 
@@ -775,14 +780,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_init(&stage_full[i], 1);
       ptx::mbar_init(&stage_empty[i], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&s_full[b], 1);
-      ptx::mbar_init(&s_free[b], kEltThreads);
-    }
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&s_full[b], 1);
     ptx::mbar_init(dp_full, 1);
-    ptx::mbar_init(dp_free, kEltThreads);
-    ptx::mbar_init(p_ready, kEltThreads);
-    ptx::mbar_init(pd_free, 1);
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&p_ready[b], kEltThreads);
+    ptx::mbar_init(ds_ready, kEltThreads);
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(mma_done, 1);
     ptx::fence_mbarrier_init();
@@ -834,50 +835,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kRows, kRows, false, false);
-    constexpr uint32_t idG = ptx::make_idesc_f16(BF16, kRows, 64, true, true);
-    const uint32_t sK = ptx::smem_u32(smem + OFF_K);
-    const uint32_t sV = ptx::smem_u32(smem + OFF_V);
+    constexpr uint32_t idG = ptx::make_idesc_f16(BF16, kRows, 64, false, true);
     const uint32_t sR = ptx::smem_u32(smem + OFF_RING);
-    const uint64_t dK = ptx::make_sdesc_sw128(sK, 16, 1024);
-    const uint64_t dV = ptx::make_sdesc_sw128(sV, 16, 1024);
-    const uint64_t dPm = ptx::make_sdesc_sw128(ptx::smem_u32(smem + OFF_P), kTile, 1024);
-    const uint64_t dSm = ptx::make_sdesc_sw128(ptx::smem_u32(smem + OFF_DS), kTile, 1024);
+    const uint64_t dK = ptx::make_sdesc_sw128(ptx::smem_u32(smem + OFF_K), 16, 1024);
+    const uint64_t dV = ptx::make_sdesc_sw128(ptx::smem_u32(smem + OFF_V), 16, 1024);
     auto stage_desc = [&](int slot, int which, bool mn) {
       return ptx::make_sdesc_sw128(sR + slot * kStageBytes + which * kTile, mn ? kTile : 16, 1024);
     };
-    auto issue_s = [&](int b, int slot) {
-      const uint64_t a0 = stage_desc(slot, 0, false);
+    // S^T (which = 0: K against Q) or dP^T (which = 1: V against dO)
+    auto issue_score = [&](int which, uint32_t d_col, int slot, uint64_t* bar) {
+      const uint64_t a0 = which == 0 ? dK : dV;
+      const uint64_t b0 = stage_desc(slot, which, false);
       if (ptx::elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_f16_ss(tmem + COL_S + b * 128, a0 + kk * 2, dK + kk * 2, idS, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(&s_full[b]);
+          ptx::mma_f16_ss(tmem + d_col, a0 + kk * 2, b0 + kk * 2, idS, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar);
       }
       __syncwarp();
     };
-    auto issue_dp = [&](int slot) {
-      const uint64_t a0 = stage_desc(slot, 1, false);
-      if (ptx::elect_one_sync()) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_f16_ss(tmem + COL_DP, a0 + kk * 2, dV + kk * 2, idS, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(dp_full);
-      }
-      __syncwarp();
-    };
-    auto issue_grads = [&](int slot, bool first) {
-      const uint64_t bq = stage_desc(slot, 0, true);
-      const uint64_t bo = stage_desc(slot, 1, true);
+    // dV += P^T dO (a_col = the P buffer) or dK += dS^T Q (a_col = dP's)
+    auto issue_grad = [&](uint32_t acc_col, uint32_t a_col, int slot, int which, bool first) {
+      const uint64_t b0 = stage_desc(slot, which, true);
       if (ptx::elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < kRows / 16; ++kk) {
+          // queries 16kk..16kk+15: warp half kk/4, 16-bit pairs from column 8*(kk%4)
+          const uint32_t a = tmem + a_col + (kk >> 2) * 64 + (kk & 3) * 8;
           const uint64_t step = static_cast<uint64_t>(kk * 16 * 128) >> 4;  // 16 query rows
-          const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
-          ptx::mma_f16_ss(tmem + COL_DV, dPm + step, bo + step, idG, acc);
-          ptx::mma_f16_ss(tmem + COL_DK, dSm + step, bq + step, idG, acc);
+          ptx::mma_f16_ts(tmem + acc_col, a, b0 + step, idG, (kk > 0 || !first) ? 1u : 0u);
         }
-        ptx::mma_commit(pd_free);
-        ptx::mma_commit(&stage_empty[slot]);
       }
       __syncwarp();
     };
@@ -891,31 +878,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = wait(&stage_full[i], 0, kSiteMmaStage);
       if (!ok) break;
       ptx::tc_fence_after();
-      issue_s(i, i);
-      if (i == 0) issue_dp(0);
+      issue_score(0, COL_S + i * 128, i, &s_full[i]);
+      if (i == 0) issue_score(1, COL_DP, 0, dp_full);
     }
     for (int it = 0; ok && it < n; ++it) {
-      if (it + 1 < n) {
-        // dP of the next tile once the warps have loaded this tile's dP (its
-        // stage was waited for with its scores)
-        ok = wait(dp_free, it & 1, kSiteMmaSFree);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        issue_dp((it + 1) % ST);
-      }
-      ok = wait(p_ready, it & 1, kSiteMmaP);
+      const int b = it & 1;
+      const int slot = it % ST;
+      ok = wait(&p_ready[b], (it >> 1) & 1, kSiteMmaP);
       if (!ok) break;
       ptx::tc_fence_after();
-      issue_grads(it % ST, it == 0);
+      issue_grad(COL_DV, COL_S + b * 128, slot, 1, it == 0);
+      ok = wait(ds_ready, it & 1, kSiteMmaP);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_grad(COL_DK, COL_DP, slot, 0, it == 0);
+      if (ptx::elect_one_sync()) ptx::mma_commit(&stage_empty[slot]);
+      __syncwarp();
+      // the next tile's stage was waited for with its scores
+      if (it + 1 < n) issue_score(1, COL_DP, (it + 1) % ST, dp_full);
       if (it + 2 < n) {
-        const int b = it & 1;
-        ok = wait(&s_free[b], (it >> 1) & 1, kSiteMmaSFree);
-        if (!ok) break;
         const int s2 = (it + 2) % ST;
         ok = wait(&stage_full[s2], ((it + 2) / ST) & 1, kSiteMmaStage);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_s(b, s2);
+        issue_score(0, COL_S + b * 128, s2, &s_full[b]);
       }
     }
     // every MMA issued must be complete before TMEM is freed
@@ -928,100 +914,91 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ---------------------------------------------------------------- elementwise
     const int quarter = warp & 3;                    // TMEM lanes 32*quarter..
-    const int half = warp >> 2;                      // keys 64*half.. of the tile
-    const int row = quarter * 32 + lane;             // query row of a streamed tile
+    const int half = warp >> 2;                      // queries 64*half.. of each tile
+    const int row = quarter * 32 + lane;             // key within the tile
+    const int key = w.r0 + row;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float2 sl2 = make_float2(scale_log2, scale_log2);
-    const int k0 = w.r0 + half * 64;                 // first key of this thread's 64
     bool ok = true;
     for (int it = 0; ok && it < n; ++it) {
       const int b = it & 1;
       const int slot = it % ST;
       ok = ptx::mbar_wait(&s_full[b], (it >> 1) & 1, status, status_word(kKern, kSiteEltS));
-      if (ok) ok = ptx::mbar_wait(dp_full, it & 1, status, status_word(kKern, kSiteEltS));
+      // the row vectors arrived with the tile (TMA writes are visible to the
+      // threads that observe the stage barrier)
       if (ok)
         ok = ptx::mbar_wait(&stage_full[slot], (it / ST) & 1, status,
                             status_word(kKern, kSiteEltStage));
+      // tcgen05.ld/st/wait are warp-collective: the whole warp takes every
+      // branch around them
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
       int sbh, s0;
       item_of(w, it, &sbh, &s0);
-      const uint8_t* stg = smem + OFF_RING + slot * kStageBytes;
-      const float l2 = reinterpret_cast<const float*>(stg + 2 * kTile)[row];
-      const float dd = reinterpret_cast<const float*>(stg + 2 * kTile + kRows * 4)[row];
-      const float2 nl = make_float2(-l2, -l2);
-      const float2 nd = make_float2(-dd, -dd);
-      // keys k0 + c visible: c <= cmax (causal, and keys past T_kv)
-      const int q = s0 + row;
-      const int cmax = min(T_kv - 1, causal ? q + off : T_kv - 1) - k0;
-      const bool all_visible = __all_sync(0xffffffffu, cmax >= 63);
-      // S and dP of the thread's 64 keys, all loaded before any use; the
-      // buffers are released at once (the next products may overwrite them)
-      uint32_t sr[128];
-      ptx::tmem_ld_32x32b_x32(t_lane + COL_S + b * 128 + half * 64,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_ld_32x32b_x32(t_lane + COL_DP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      ptx::tmem_ld_32x32b_x32(t_lane + COL_S + b * 128 + half * 64 + 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      ptx::tmem_ld_32x32b_x32(t_lane + COL_DP + half * 64 + 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      tmem_wait_ld_64(*reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
-      tmem_wait_ld_64(*reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&s_free[b]);
-      ptx::mbar_arrive(dp_free);
-      uint8_t* prow = smem + OFF_P + half * kTile + row * 128;
-      uint8_t* grow = smem + OFF_DS + half * kTile + row * 128;
+      const float4* lv = reinterpret_cast<const float4*>(smem + OFF_RING + slot * kStageBytes +
+                                                         2 * kTile) + half * 16;
+      const float4* dv4 = lv + kRows / 4;
+      // query s0 + 64*half + c sees this key iff c >= cmin
+      int cmin = causal ? key - off - (s0 + half * 64) : INT_MIN / 2;
+      if (key >= T_kv) cmin = 64;  // key past the end: nothing visible
+      const bool all_visible = __all_sync(0xffffffffu, cmin <= 0);
+      const uint32_t t_s = t_lane + COL_S + b * 128 + half * 64;
+      const uint32_t t_dp = t_lane + COL_DP + half * 64;
+      uint32_t sr[64];
+      ptx::tmem_ld_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      ptx::tmem_ld_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_wait_ld_64(sr);
+      const float* s = reinterpret_cast<const float*>(sr);
+      float2 pp[32];
 #pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        const float* s = reinterpret_cast<const float*>(sr + c32 * 64);
-        const float* dp = reinterpret_cast<const float*>(sr + c32 * 64 + 32);
-        float2 pp[16];
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l = lv[c4];
+        const float2 x0 = __ffma2_rn(make_float2(s[4 * c4], s[4 * c4 + 1]), sl2, make_float2(-l.x, -l.y));
+        const float2 x1 =
+            __ffma2_rn(make_float2(s[4 * c4 + 2], s[4 * c4 + 3]), sl2, make_float2(-l.z, -l.w));
+        pp[2 * c4] = make_float2(ptx::ex2_approx(x0.x), ptx::ex2_approx(x0.y));
+        pp[2 * c4 + 1] = make_float2(ptx::ex2_approx(x1.x), ptx::ex2_approx(x1.y));
+      }
+      if (!all_visible) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 x = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), sl2, nl);
-          pp[j] = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-        }
-        if (!all_visible) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int c = c32 * 32 + 2 * j;
-            pp[j].x = c <= cmax ? pp[j].x : 0.f;
-            pp[j].y = c + 1 <= cmax ? pp[j].y : 0.f;
-          }
-        }
-        uint32_t pk[16], gk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 g = __fmul2_rn(pp[j], __fadd2_rn(make_float2(dp[2 * j], dp[2 * j + 1]), nd));
-          pk[j] = pack2<BF16>(pp[j].x, pp[j].y);
-          gk[j] = pack2<BF16>(g.x, g.y);
-        }
-        if (c32 == 0 && it >= 1) {
-          // the previous tile's gradient products read the P and dS rows
-          bool good = ptx::mbar_wait(pd_free, (it - 1) & 1, status, status_word(kKern, kSiteEltStage));
-          good = __all_sync(0xffffffffu, good);
-          if (!good) {
-            ok = false;
-            break;
-          }
-        }
-        // this half's 32 keys of the query's P and dS rows: chunks 4*c32 ..
-        // 4*c32+3 of 16 bytes, chunk c at position c ^ (row % 8)
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int pos = ((c32 * 4 + c4) ^ (row & 7)) << 4;
-          *reinterpret_cast<uint4*>(prow + pos) =
-              make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-          *reinterpret_cast<uint4*>(grow + pos) =
-              make_uint4(gk[4 * c4], gk[4 * c4 + 1], gk[4 * c4 + 2], gk[4 * c4 + 3]);
+        for (int c = 0; c < 64; c += 2) {
+          pp[c >> 1].x = c >= cmin ? pp[c >> 1].x : 0.f;
+          pp[c >> 1].y = c + 1 >= cmin ? pp[c >> 1].y : 0.f;
         }
       }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack2<BF16>(pp[c].x, pp[c].y);
+      ptx::tmem_st_32x32b_x32(t_s, pk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&p_ready[b]);
+
+      ok = ptx::mbar_wait(dp_full, it & 1, status, status_word(kKern, kSiteEltS));
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      // generic-proxy writes, read next by the tensor core
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(p_ready);
+      ptx::tc_fence_after();
+      uint32_t dr[64];
+      ptx::tmem_ld_32x32b_x32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      ptx::tmem_ld_32x32b_x32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_wait_ld_64(dr);
+      const float* dp = reinterpret_cast<const float*>(dr);
+      uint32_t gk[32];
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 dd = dv4[c4];
+        const float2 g0 = __fmul2_rn(pp[2 * c4], __fadd2_rn(make_float2(dp[4 * c4], dp[4 * c4 + 1]),
+                                                             make_float2(-dd.x, -dd.y)));
+        const float2 g1 = __fmul2_rn(pp[2 * c4 + 1], __fadd2_rn(make_float2(dp[4 * c4 + 2], dp[4 * c4 + 3]),
+                                                                 make_float2(-dd.z, -dd.w)));
+        gk[2 * c4] = pack2<BF16>(g0.x, g0.y);
+        gk[2 * c4 + 1] = pack2<BF16>(g1.x, g1.y);
+      }
+      ptx::tmem_st_32x32b_x32(t_dp, gk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ds_ready);
     }
     if (ok) {
       // -------------------------------------------------------------- epilogue
@@ -1029,8 +1006,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         ptx::tc_fence_after();
-        const int key = w.r0 + row;  // accumulator lanes are keys
-        const bool write = key < T_kv;
+        const bool write = key < T_kv;  // accumulator lanes are keys
 #pragma unroll
         for (int a = 0; a < 2; ++a) {
           uint8_t* dst = reinterpret_cast<uint8_t*>(a == 0 ? dv_out : dk_out) +
@@ -1065,6 +1041,338 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// dQ at d = 64 with 128-key streamed tiles. One CTA per (query head, 128-row
+// query tile), heaviest first: Q and dO stay (copied once into TMEM as the A
+// operands of the score products) and the CTA streams 128-key tiles of K and
+// V through a 5-stage ring, causally up to the diagonal. The query rows sit on
+// the TMEM lanes; per key tile t the tensor core computes
+//   S_t = Q K_t^T and dP_t = dO V_t^T   (M = 128 rows, N = 128 keys, K = 64)
+// with A from TMEM and B from shared memory, S into one buffer and dP into
+// one of two. Elementwise thread (warp w, lane i) owns row 32*(w%4)+i (its
+// lse and D are two registers) and the 64 keys 64*(w/4).. of each tile: it
+// loads its S values and releases the S buffer at once, forms P, waits for
+// dP, forms dS = P * (dP - D) and stores it as 16-bit pairs over the first
+// 32 of its 64 dP columns; the tensor core accumulates dQ += dS_t K_t (M =
+// 128 rows, N = 64, K = 128 keys; A from TMEM, B the K tile read MN-major).
+// Issue order per tile: S(t+1) once S(t) is loaded, then dQ(t) once dS(t) is
+// stored, then dP(t+2) into the buffer dQ(t) has just read (one thread's
+// MMAs execute in order), so the scores of a tile are ready before the warps
+// reach it. TMEM: S [0,128), dP [128,384), dQ [384,448), Q [448,480),
+// dO [480,512).
+// ---------------------------------------------------------------------------
+namespace q128 {
+constexpr int kRows = 128;                // query rows per CTA; keys per streamed tile
+constexpr int kTile = kRows * 64 * 2;     // one [128 rows][64] 16-bit tile (128-byte rows)
+constexpr int kStages = 5;
+constexpr int kStageBytes = 2 * kTile;    // K, V
+constexpr int OFF_Q = 0;
+constexpr int OFF_DO = kTile;
+constexpr int OFF_RING = 2 * kTile;
+constexpr int OFF_BAR = OFF_RING + kStages * kStageBytes;
+// res_full, res_tmem, stage_full[5], stage_empty[5], s_full, s_free, dp_full[2], ds_ready[2],
+// acc_full, mma_done
+constexpr int N_BARS = 2 + 2 * kStages + 2 + 4 + 2;
+constexpr int OFF_TMEMPTR = OFF_BAR + N_BARS * 8;
+constexpr int SMEM_BYTES = OFF_TMEMPTR + 16 + 1024;  // + alignment slack
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 384, COL_Q = 448, COL_DO = 480;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+}  // namespace q128
+
+template <bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_q128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const float* __restrict__ ws_l2, const float* __restrict__ ws_dd, int Tq_pad,
+                    void* __restrict__ dq_out, int T_q, int T_kv, int BH, int n_qt, int h, int h_kv,
+                    float scale, float scale_log2, int causal, unsigned int* __restrict__ status) {
+  using namespace q128;
+  constexpr int ST = kStages;
+  constexpr uint32_t kKern = kKernBwdQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* res_tmem = bars + 1;
+  uint64_t* stage_full = bars + 2;
+  uint64_t* stage_empty = stage_full + ST;
+  uint64_t* s_full = stage_empty + ST;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* dp_full = s_free + 1;   // [2]
+  uint64_t* ds_ready = dp_full + 2;  // [2]
+  uint64_t* acc_full = ds_ready + 2;
+  uint64_t* mma_done = acc_full + 1;
+  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + OFF_TMEMPTR);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int group = h / h_kv;
+  const int off = T_kv - T_q;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int r0 = (n_qt - 1 - static_cast<int>(blockIdx.x) / BH) * kRows;
+  const int kv_bh = bh / group;  // (b * h + i) / group = b * h_kv + i / group
+  const int last_row = min(T_q, r0 + kRows) - 1;
+  const int last_key = causal ? min(T_kv - 1, last_row + off) : T_kv - 1;  // >= 0: T_q <= T_kv
+  const int n = last_key / kRows + 1;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(res_full, 1);
+    ptx::mbar_init(res_tmem, kEltThreads);
+    for (int i = 0; i < ST; ++i) {
+      ptx::mbar_init(&stage_full[i], 1);
+      ptx::mbar_init(&stage_empty[i], 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(s_free, kEltThreads);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&dp_full[b], 1);
+      ptx::mbar_init(&ds_ready[b], kEltThreads);
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(mma_done, 1);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == kWarpMma) {
+    ptx::tmem_alloc(tmem_ptr, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == kWarpProd) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmQ);
+      ptx::prefetch_tensormap(&tmO);
+      ptx::prefetch_tensormap(&tmK);
+      ptx::prefetch_tensormap(&tmV);
+      // the streamed tiles are read by every query tile of the head: keep
+      // them in L2; the resident ones once
+      const uint64_t pol_str = ptx::policy_evict_last();
+      const uint64_t pol_res = ptx::policy_evict_first();
+      ptx::mbar_arrive_expect_tx(res_full, 2 * kTile);
+      ptx::tma_load_3d(smem + OFF_Q, &tmQ, res_full, 0, r0, bh, pol_res);
+      ptx::tma_load_3d(smem + OFF_DO, &tmO, res_full, 0, r0, bh, pol_res);
+      bool ok = true;
+      int it = 0;
+      for (; it < n; ++it) {
+        const int slot = it % ST;
+        ok = ptx::mbar_wait(&stage_empty[slot], ((it / ST) & 1) ^ 1, status,
+                            status_word(kKern, kSiteProdStage));
+        if (!ok) break;
+        uint8_t* stg = smem + OFF_RING + slot * kStageBytes;
+        ptx::mbar_arrive_expect_tx(&stage_full[slot], 2 * kTile);
+        ptx::tma_load_3d(stg, &tmK, &stage_full[slot], 0, it * kRows, kv_bh, pol_str);
+        ptx::tma_load_3d(stg + kTile, &tmV, &stage_full[slot], 0, it * kRows, kv_bh, pol_str);
+      }
+      if (!ok) {
+        // let the copies in flight land before the CTA's shared memory goes
+        mbar_drain(res_full, 0);
+        for (int i = (it > ST ? it - ST : 0); i < it; ++i) mbar_drain(&stage_full[i % ST], (i / ST) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idS = ptx::make_idesc_f16(BF16, kRows, kRows, false, false);
+    constexpr uint32_t idG = ptx::make_idesc_f16(BF16, kRows, 64, false, true);
+    const uint32_t sR = ptx::smem_u32(smem + OFF_RING);
+    auto stage_desc = [&](int slot, int which, bool mn) {
+      return ptx::make_sdesc_sw128(sR + slot * kStageBytes + which * kTile, mn ? kTile : 16, 1024);
+    };
+    // S (which = 0: Q against K) or dP (which = 1: dO against V)
+    auto issue_score = [&](int which, uint32_t d_col, int slot, uint64_t* bar) {
+      const uint32_t a0 = tmem + (which == 0 ? COL_Q : COL_DO);
+      const uint64_t b0 = stage_desc(slot, which, false);
+      if (ptx::elect_one_sync()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_f16_ts(tmem + d_col, a0 + kk * 8, b0 + kk * 2, idS, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar);
+      }
+      __syncwarp();
+    };
+    // dQ += dS K, dS over the first 32 columns of each half of dP buffer b
+    auto issue_dq = [&](int b, int slot, bool first) {
+      const uint64_t b0 = stage_desc(slot, 0, true);
+      if (ptx::elect_one_sync()) {
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk) {
+          // keys 16kk..16kk+15: warp half kk/4, 16-bit pairs from column 8*(kk%4)
+          const uint32_t a = tmem + COL_DP + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+          const uint64_t step = static_cast<uint64_t>(kk * 16 * 128) >> 4;  // 16 key rows
+          ptx::mma_f16_ts(tmem + COL_DQ, a, b0 + step, idG, (kk > 0 || !first) ? 1u : 0u);
+        }
+        ptx::mma_commit(&stage_empty[slot]);
+      }
+      __syncwarp();
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      const bool good = ptx::mbar_wait(bar, parity, status, status_word(kKern, site));
+      return __all_sync(0xffffffffu, good);
+    };
+
+    bool ok = wait(res_tmem, 0, kSiteMmaRes);
+    for (int i = 0; ok && i < 2 && i < n; ++i) {
+      ok = wait(&stage_full[i], 0, kSiteMmaStage);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (i == 0) issue_score(0, COL_S, 0, s_full);
+      issue_score(1, COL_DP + i * 128, i, &dp_full[i]);
+    }
+    for (int it = 0; ok && it < n; ++it) {
+      const int b = it & 1;
+      if (it + 1 < n) {
+        // S(it+1) once the warps hold S(it); its stage was waited for with dP
+        ok = wait(s_free, it & 1, kSiteMmaSFree);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_score(0, COL_S, (it + 1) % ST, s_full);
+      }
+      ok = wait(&ds_ready[b], (it >> 1) & 1, kSiteMmaP);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_dq(b, it % ST, it == 0);
+      if (it + 2 < n) {
+        const int s2 = (it + 2) % ST;
+        ok = wait(&stage_full[s2], ((it + 2) / ST) & 1, kSiteMmaStage);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_score(1, COL_DP + b * 128, s2, &dp_full[b]);
+      }
+    }
+    // every MMA issued must be complete before TMEM is freed
+    if (ptx::elect_one_sync()) {
+      if (ok) ptx::mma_commit(acc_full);
+      ptx::mma_commit(mma_done);
+    }
+    __syncwarp();
+    mbar_drain(mma_done, 0);
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    const int quarter = warp & 3;                    // TMEM lanes 32*quarter..
+    const int half = warp >> 2;                      // keys 64*half.. of each tile
+    const int row = quarter * 32 + lane;             // query row within the tile
+    const int q = r0 + row;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const size_t ro = static_cast<size_t>(bh) * Tq_pad + q;  // q < Tq_pad
+    const float l2 = ws_l2[ro];
+    const float dd = ws_dd[ro];
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
+    const float2 nl = make_float2(-l2, -l2);
+    const float2 nd = make_float2(-dd, -dd);
+    const int kmax = causal ? min(T_kv - 1, q + off) : T_kv - 1;  // last key this row sees
+    bool ok = ptx::mbar_wait(res_full, 0, status, status_word(kKern, kSiteEltRes));
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      // row `row` of Q (warps 0-3) or dO (warps 4-7), from the 128-byte
+      // swizzled tile (16-byte chunk c of row r sits at chunk c ^ (r % 8)),
+      // into 32 TMEM columns as 16-bit pairs in K order: the A operand of the
+      // score products
+      const uint8_t* src = smem + (half ? OFF_DO : OFF_Q) + row * 128;
+      uint32_t words[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
+        words[4 * c] = v.x;
+        words[4 * c + 1] = v.y;
+        words[4 * c + 2] = v.z;
+        words[4 * c + 3] = v.w;
+      }
+      ptx::tmem_st_32x32b_x32(t_lane + (half ? COL_DO : COL_Q), words);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(res_tmem);
+    }
+    for (int it = 0; ok && it < n; ++it) {
+      const int b = it & 1;
+      ok = ptx::mbar_wait(s_full, it & 1, status, status_word(kKern, kSiteEltS));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int k0 = it * kRows + half * 64;
+      const int cmax = kmax - k0;  // keys k0 + c with c <= cmax are visible
+      const bool all_visible = __all_sync(0xffffffffu, cmax >= 63);
+      uint32_t sr[64];
+      ptx::tmem_ld_32x32b_x32(t_lane + COL_S + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      ptx::tmem_ld_32x32b_x32(t_lane + COL_S + half * 64 + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_wait_ld_64(sr);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(s_free);
+      const float* s = reinterpret_cast<const float*>(sr);
+      float2 pp[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float2 x = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), sl2, nl);
+        pp[j] = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+      }
+      if (!all_visible) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          pp[j].x = 2 * j <= cmax ? pp[j].x : 0.f;
+          pp[j].y = 2 * j + 1 <= cmax ? pp[j].y : 0.f;
+        }
+      }
+      ok = ptx::mbar_wait(&dp_full[b], (it >> 1) & 1, status, status_word(kKern, kSiteEltS));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_dp = t_lane + COL_DP + b * 128 + half * 64;
+      uint32_t dr[64];
+      ptx::tmem_ld_32x32b_x32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      ptx::tmem_ld_32x32b_x32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_wait_ld_64(dr);
+      const float* dp = reinterpret_cast<const float*>(dr);
+      uint32_t gk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float2 g = __fmul2_rn(pp[j], __fadd2_rn(make_float2(dp[2 * j], dp[2 * j + 1]), nd));
+        gk[j] = pack2<BF16>(g.x, g.y);
+      }
+      ptx::tmem_st_32x32b_x32(t_dp, gk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ds_ready[b]);
+    }
+    if (ok) {
+      // -------------------------------------------------------------- epilogue
+      ok = ptx::mbar_wait(acc_full, 0, status, status_word(kKern, kSiteEltAcc));
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        ptx::tc_fence_after();
+        const bool write = q < T_q;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(dq_out) +
+                       (static_cast<size_t>(bh) * T_q + (write ? q : 0)) * 64 * 2 + half * 32 * 2;
+        uint32_t raw[32];
+        ptx::tmem_ld_32x32b_x32(t_lane + COL_DQ + half * 32, raw);
+        tmem_wait_ld_32(raw);
+        if (write) {
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const float* f = reinterpret_cast<const float*>(&raw[g8 * 8]);
+            uint4 v;
+            v.x = pack2<BF16>(f[0] * scale, f[1] * scale);
+            v.y = pack2<BF16>(f[2] * scale, f[3] * scale);
+            v.z = pack2<BF16>(f[4] * scale, f[5] * scale);
+            v.w = pack2<BF16>(f[6] * scale, f[7] * scale);
+            *reinterpret_cast<uint4*>(dst + g8 * 16) = v;
+          }
+        }
+      }
+    }
+    ptx::tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == kWarpMma) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
 template <typename K>
 cudaError_t configure_once(K kern, int smem_bytes, uint64_t* configured, int dev) {
   if (dev >= 64 || (*configured & (1ull << dev))) return cudaSuccess;
@@ -1073,21 +1381,39 @@ cudaError_t configure_once(K kern, int smem_bytes, uint64_t* configured, int dev
   return e;
 }
 
+// The two gradient kernels of one head dimension: at d = 64 the 128-row
+// streamed tiles (bwd_kv128_kernel, bwd_q128_kernel), at d = 128 bwd_kernel
+// in its two modes with 64-row streamed tiles.
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdProblem& p, cudaStream_t stream) {
-  using CK = BwdCfg<D, true>;
-  using CQ = BwdCfg<D, false>;
-  auto kern_kv = bwd_kernel<D, BF16, true>;
-  auto kern_q = bwd_kernel<D, BF16, false>;
   static std::mutex mu;
   static uint64_t conf_kv = 0, conf_q = 0;  // one bit per device ordinal
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  constexpr bool k128 = D == 64;
+  constexpr int kv_str = k128 ? kv128::kRows : kStr;
+  constexpr int q_str = k128 ? q128::kRows : kStr;
+  constexpr int kv_smem = [] {
+    if constexpr (k128) return kv128::SMEM_BYTES;
+    else return BwdCfg<D, true>::SMEM_BYTES;
+  }();
+  constexpr int q_smem = [] {
+    if constexpr (k128) return q128::SMEM_BYTES;
+    else return BwdCfg<D, false>::SMEM_BYTES;
+  }();
+  auto kern_kv = [] {
+    if constexpr (k128) return bwd_kv128_kernel<BF16>;
+    else return bwd_kernel<D, BF16, true>;
+  }();
+  auto kern_q = [] {
+    if constexpr (k128) return bwd_q128_kernel<BF16>;
+    else return bwd_kernel<D, BF16, false>;
+  }();
   {
     std::lock_guard<std::mutex> g(mu);
-    e = configure_once(kern_kv, CK::SMEM_BYTES, &conf_kv, dev);
-    if (e == cudaSuccess) e = configure_once(kern_q, CQ::SMEM_BYTES, &conf_q, dev);
+    e = configure_once(kern_kv, kv_smem, &conf_kv, dev);
+    if (e == cudaSuccess) e = configure_once(kern_q, q_smem, &conf_q, dev);
     if (e != cudaSuccess) return e;
   }
   const int BH = p.B * p.h;
@@ -1106,50 +1432,40 @@ cudaError_t launch_bwd_t(const BwdProblem& p, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  // 2. dK, dV: resident K/V tiles, streamed Q/dO tiles
+  // 2. dK, dV: resident 128-key K/V tiles, streamed Q/dO tiles
   CUtensorMap mX, mY, mU, mW;
-  if constexpr (D == 64) {
-    // the streamed queries on the TMEM lanes (bwd_kvq_kernel)
-    auto kern_kvq = bwd_kvq_kernel<BF16>;
-    static uint64_t conf_kvq = 0;
-    {
-      std::lock_guard<std::mutex> g(mu);
-      e = configure_once(kern_kvq, kvq::SMEM_BYTES, &conf_kvq, dev);
-      if (e != cudaSuccess) return e;
-    }
-    if (!make_map(&mX, p.k, p.T_kv, BH_kv, D, BF16, kvq::kRows) ||
-        !make_map(&mY, p.v, p.T_kv, BH_kv, D, BF16, kvq::kRows) ||
-        !make_map(&mU, p.q, p.T_q, BH, D, BF16, kvq::kRows) ||
-        !make_map(&mW, p.dout, p.T_q, BH, D, BF16, kvq::kRows))
-      return cudaErrorInvalidValue;
-    const int n_kt = (p.T_kv + kvq::kRows - 1) / kvq::kRows;
-    kern_kvq<<<static_cast<unsigned>(BH_kv) * n_kt, kBwdThreads, kvq::SMEM_BYTES, stream>>>(
-        mX, mY, mU, mW, l2, dd, Tq_pad, p.dv, p.dk, p.T_q, p.T_kv, BH_kv, p.h, p.h_kv, p.scale,
-        scale_log2, p.causal, p.status);
-  } else {
   if (!make_map(&mX, p.k, p.T_kv, BH_kv, D, BF16, kRes) ||
       !make_map(&mY, p.v, p.T_kv, BH_kv, D, BF16, kRes) ||
-      !make_map(&mU, p.q, p.T_q, BH, D, BF16, kStr) ||
-      !make_map(&mW, p.dout, p.T_q, BH, D, BF16, kStr))
+      !make_map(&mU, p.q, p.T_q, BH, D, BF16, kv_str) ||
+      !make_map(&mW, p.dout, p.T_q, BH, D, BF16, kv_str))
     return cudaErrorInvalidValue;
   const int n_kt = (p.T_kv + kRes - 1) / kRes;
-  kern_kv<<<static_cast<unsigned>(BH_kv) * n_kt, kBwdThreads, CK::SMEM_BYTES, stream>>>(
-      mX, mY, mU, mW, l2, dd, Tq_pad, p.dv, p.dk, p.T_q, p.T_kv, BH_kv, n_kt, p.h, p.h_kv, p.scale,
-      scale_log2, p.causal, p.status);
-  }
+  if constexpr (k128)
+    kern_kv<<<static_cast<unsigned>(BH_kv) * n_kt, kBwdThreads, kv_smem, stream>>>(
+        mX, mY, mU, mW, l2, dd, Tq_pad, p.dv, p.dk, p.T_q, p.T_kv, BH_kv, p.h, p.h_kv, p.scale,
+        scale_log2, p.causal, p.status);
+  else
+    kern_kv<<<static_cast<unsigned>(BH_kv) * n_kt, kBwdThreads, kv_smem, stream>>>(
+        mX, mY, mU, mW, l2, dd, Tq_pad, p.dv, p.dk, p.T_q, p.T_kv, BH_kv, n_kt, p.h, p.h_kv,
+        p.scale, scale_log2, p.causal, p.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  // 3. dQ: resident Q/dO tiles, streamed K/V tiles
+  // 3. dQ: resident 128-row Q/dO tiles, streamed K/V tiles
   if (!make_map(&mX, p.q, p.T_q, BH, D, BF16, kRes) ||
       !make_map(&mY, p.dout, p.T_q, BH, D, BF16, kRes) ||
-      !make_map(&mU, p.k, p.T_kv, BH_kv, D, BF16, kStr) ||
-      !make_map(&mW, p.v, p.T_kv, BH_kv, D, BF16, kStr))
+      !make_map(&mU, p.k, p.T_kv, BH_kv, D, BF16, q_str) ||
+      !make_map(&mW, p.v, p.T_kv, BH_kv, D, BF16, q_str))
     return cudaErrorInvalidValue;
   const int n_qt = (p.T_q + kRes - 1) / kRes;
-  kern_q<<<static_cast<unsigned>(BH) * n_qt, kBwdThreads, CQ::SMEM_BYTES, stream>>>(
-      mX, mY, mU, mW, l2, dd, Tq_pad, nullptr, p.dq, p.T_q, p.T_kv, BH, n_qt, p.h, p.h_kv, p.scale,
-      scale_log2, p.causal, p.status);
+  if constexpr (k128)
+    kern_q<<<static_cast<unsigned>(BH) * n_qt, kBwdThreads, q_smem, stream>>>(
+        mX, mY, mU, mW, l2, dd, Tq_pad, p.dq, p.T_q, p.T_kv, BH, n_qt, p.h, p.h_kv, p.scale,
+        scale_log2, p.causal, p.status);
+  else
+    kern_q<<<static_cast<unsigned>(BH) * n_qt, kBwdThreads, q_smem, stream>>>(
+        mX, mY, mU, mW, l2, dd, Tq_pad, nullptr, p.dq, p.T_q, p.T_kv, BH, n_qt, p.h, p.h_kv,
+        p.scale, scale_log2, p.causal, p.status);
   return cudaGetLastError();
 }
 
