@@ -680,10 +680,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // tensor core computes
 //   S_t^T = K Q_t^T and dP_t^T = V dO_t^T   (M = 128 keys, N = 128 queries, K = 64)
 // from shared memory into TMEM (S in two buffers, dP in one). Elementwise
-// thread (warp w, lane i) owns key 32*(w%4)+i and the 64 queries 64*(w/4)..
-// of each tile, whose lse and D it reads from the stage as broadcasts. It
+// warp w owns the keys 32*(w%4).. (its TMEM lane quarter) and the 64 queries
+// 64*(w/4).. of each tile. It reads them with the 16-lane shape: each thread
+// holds four keys (lanes i/4 + {0, 8, 16, 24}) at 16 of the columns (two of
+// every eight), so it needs only those 16 columns' lse and D from the stage
+// (8-byte loads that four lanes share) rather than all 64 in every lane. It
 // forms P = 2^(scale*log2e*S - lse*log2e) and stores it as 16-bit pairs over
-// the first 32 of its 64 S columns; once dP is there it forms
+// the first 32 of its 64 S columns (16x128b shape: the pair of columns
+// 8r + 2(i%4) is word 4r + i%4 of the lane); once dP is there it forms
 // dS = P * (dP - D) and stores it the same way over its dP columns. The
 // tensor core accumulates dV += P_t^T dO_t and dK += dS_t^T Q_t (M = 128
 // keys, N = 64, K = 128 queries) with A read from TMEM and B the streamed
@@ -915,8 +919,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ---------------------------------------------------------------- elementwise
     const int quarter = warp & 3;                    // TMEM lanes 32*quarter..
     const int half = warp >> 2;                      // queries 64*half.. of each tile
-    const int row = quarter * 32 + lane;             // key within the tile
-    const int key = w.r0 + row;
+    const int key = w.r0 + quarter * 32 + lane;      // the epilogue's key (32x32b shape)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float2 sl2 = make_float2(scale_log2, scale_log2);
     bool ok = true;
@@ -936,41 +939,73 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_after();
       int sbh, s0;
       item_of(w, it, &sbh, &s0);
-      const float4* lv = reinterpret_cast<const float4*>(smem + OFF_RING + slot * kStageBytes +
-                                                         2 * kTile) + half * 16;
-      const float4* dv4 = lv + kRows / 4;
-      // query s0 + 64*half + c sees this key iff c >= cmin
-      int cmin = causal ? key - off - (s0 + half * 64) : INT_MIN / 2;
-      if (key >= T_kv) cmin = 64;  // key past the end: nothing visible
-      const bool all_visible = __all_sync(0xffffffffu, cmin <= 0);
-      const uint32_t t_s = t_lane + COL_S + b * 128 + half * 64;
-      const uint32_t t_dp = t_lane + COL_DP + half * 64;
+      // lse*log2e and D of this thread's 16 query columns: 8r + c2 and the
+      // next, r = 0..7 (4 distinct 8-byte words per warp load)
+      const float* lvec = reinterpret_cast<const float*>(smem + OFF_RING + slot * kStageBytes +
+                                                         2 * kTile) + half * 64;
+      const float* dvec = lvec + kRows;
+      const int c2 = 2 * (lane & 3);
+      // this thread's four keys: rows 16h + lane/4 + 8e of the warp's quarter
+      // (h, e in {0, 1}); query s0 + 64*half + c sees key x iff c >= cmin[x]
+      int cmin[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int kx = w.r0 + quarter * 32 + 16 * (x >> 1) + (lane >> 2) + 8 * (x & 1);
+        cmin[x] = causal ? kx - off - (s0 + half * 64) : INT_MIN / 2;
+        if (kx >= T_kv) cmin[x] = 64;  // key past the end: nothing visible
+      }
+      const bool all_visible =
+          __all_sync(0xffffffffu, max(max(cmin[0], cmin[1]), max(cmin[2], cmin[3])) <= 0);
+      const uint32_t col_s = COL_S + b * 128 + half * 64;
+      const uint32_t col_dp = COL_DP + half * 64;
+      float2 nl[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float2 l = *reinterpret_cast<const float2*>(lvec + 8 * r + c2);
+        nl[r] = make_float2(-l.x, -l.y);
+      }
+      // S of lanes 0-15 (sr[0..31]) and 16-31 (sr[32..63]) of the quarter:
+      // sr[32h + 4r + 2e + j] = S(key (h, e), column 8r + c2 + j)
       uint32_t sr[64];
-      ptx::tmem_ld_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_ld_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      ptx::tmem_ld_16x256b_x8(t_lane + col_s, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      ptx::tmem_ld_16x256b_x8(t_lane + (16u << 16) + col_s, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld_64(sr);
       const float* s = reinterpret_cast<const float*>(sr);
+      // pp[16h + 2r + e]: key (h, e), columns 8r + c2 and 8r + c2 + 1
       float2 pp[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l = lv[c4];
-        const float2 x0 = __ffma2_rn(make_float2(s[4 * c4], s[4 * c4 + 1]), sl2, make_float2(-l.x, -l.y));
-        const float2 x1 =
-            __ffma2_rn(make_float2(s[4 * c4 + 2], s[4 * c4 + 3]), sl2, make_float2(-l.z, -l.w));
-        pp[2 * c4] = make_float2(ptx::ex2_approx(x0.x), ptx::ex2_approx(x0.y));
-        pp[2 * c4 + 1] = make_float2(ptx::ex2_approx(x1.x), ptx::ex2_approx(x1.y));
-      }
+      for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 32 * h2 + 4 * r + 2 * e;
+            const float2 x = __ffma2_rn(make_float2(s[i], s[i + 1]), sl2, nl[r]);
+            pp[16 * h2 + 2 * r + e] = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+          }
       if (!all_visible) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          pp[c >> 1].x = c >= cmin ? pp[c >> 1].x : 0.f;
-          pp[c >> 1].y = c + 1 >= cmin ? pp[c >> 1].y : 0.f;
-        }
-      }
-      uint32_t pk[32];
+        for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack2<BF16>(pp[c].x, pp[c].y);
-      ptx::tmem_st_32x32b_x32(t_s, pk);
+          for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = 8 * r + c2, m = cmin[2 * h2 + e];
+              float2& v = pp[16 * h2 + 2 * r + e];
+              v.x = c >= m ? v.x : 0.f;
+              v.y = c + 1 >= m ? v.y : 0.f;
+            }
+      }
+      // P as 16-bit pairs over the first 32 of the warp's 64 S columns: the
+      // pair of columns 8r + c2 is word 4r + lane%4, which the 16x128b shape
+      // takes from register 2r (lane lane/4) and 2r + 1 (lane lane/4 + 8)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = pack2<BF16>(pp[16 * h2 + j].x, pp[16 * h2 + j].y);
+        ptx::tmem_st_16x128b_x8(t_lane + (static_cast<uint32_t>(16 * h2) << 16) + col_s, pk);
+      }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&p_ready[b]);
@@ -979,23 +1014,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
+      float2 nd[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * r + c2);
+        nd[r] = make_float2(-d2.x, -d2.y);
+      }
       uint32_t dr[64];
-      ptx::tmem_ld_32x32b_x32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      ptx::tmem_ld_32x32b_x32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      ptx::tmem_ld_16x256b_x8(t_lane + col_dp, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      ptx::tmem_ld_16x256b_x8(t_lane + (16u << 16) + col_dp, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
       tmem_wait_ld_64(dr);
       const float* dp = reinterpret_cast<const float*>(dr);
-      uint32_t gk[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 dd = dv4[c4];
-        const float2 g0 = __fmul2_rn(pp[2 * c4], __fadd2_rn(make_float2(dp[4 * c4], dp[4 * c4 + 1]),
-                                                             make_float2(-dd.x, -dd.y)));
-        const float2 g1 = __fmul2_rn(pp[2 * c4 + 1], __fadd2_rn(make_float2(dp[4 * c4 + 2], dp[4 * c4 + 3]),
-                                                                 make_float2(-dd.z, -dd.w)));
-        gk[2 * c4] = pack2<BF16>(g0.x, g0.y);
-        gk[2 * c4 + 1] = pack2<BF16>(g1.x, g1.y);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t gk[16];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 32 * h2 + 4 * r + 2 * e;
+            const float2 g = __fmul2_rn(pp[16 * h2 + 2 * r + e],
+                                        __fadd2_rn(make_float2(dp[i], dp[i + 1]), nd[r]));
+            gk[2 * r + e] = pack2<BF16>(g.x, g.y);
+          }
+        ptx::tmem_st_16x128b_x8(t_lane + (static_cast<uint32_t>(16 * h2) << 16) + col_dp, gk);
       }
-      ptx::tmem_st_32x32b_x32(t_dp, gk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ds_ready);
