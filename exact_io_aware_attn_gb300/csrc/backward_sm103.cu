@@ -45,8 +45,9 @@
 // The scores of tile t+1 go into the other buffer while the elementwise warps
 // work on tile t. In KV mode P_t is stored and released first (its own
 // barrier), so dV += P_t^T dO_t runs while the warps form dS_t; Q mode stores
-// only dS_t. The streamed rows' lse and D are read from shared memory before
-// the TMEM loads, so their latency overlaps. TMEM: buffers [0,128) and
+// only dS_t. In KV mode the streamed rows' lse and D are per column: the
+// warps read TMEM with the 16-lane shape (each thread four keys at 8 of the
+// 32 columns), so a thread needs 8 columns' values, not 32. TMEM: buffers [0,128) and
 // [128,256) (S then dP, 64 columns each), dV at 256, dK or dQ at 256 + d:
 // 512 columns at d = 128.
 #include <cuda.h>
@@ -538,91 +539,140 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      // the streamed rows' lse and D (KV): read before the TMEM loads so
-      // their latency overlaps
-      float4 lv[8], dv4[8];
-      if constexpr (KV) {
-        const float* v0 = reinterpret_cast<const float*>(smem + C::OFF_RING +
-                                                         slot * C::STAGE_BYTES + 2 * C::STR_BYTES);
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          lv[c4] = reinterpret_cast<const float4*>(v0 + half * 32)[c4];
-          dv4[c4] = reinterpret_cast<const float4*>(v0 + kStr + half * 32)[c4];
-        }
-      } else {
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          lv[c4] = make_float4(l2_row, l2_row, l2_row, l2_row);
-          dv4[c4] = make_float4(dd_row, dd_row, dd_row, dd_row);
-        }
-      }
-      uint32_t sr[64];
-      ptx::tmem_ld_32x32b_x32(t_half + col_buf(b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_ld_32x32b_x32(t_half + col_buf(b) + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_wait_ld_64(sr);
-      const float* s = reinterpret_cast<const float*>(sr);        // scores, 32 columns
-      const float* dp = reinterpret_cast<const float*>(sr + 32);  // dP, same columns
-
       int sbh, s0;
       bwd_item(w, it, &sbh, &s0);
       s0 += half * 32;  // streamed row of this warp's column 0
-      // columns [cmin, cmax] of this row are visible
-      int cmin, cmax;
       if constexpr (KV) {
-        cmin = causal ? rrow - off - s0 : INT_MIN / 2;   // query s0+c sees key rrow iff c >= cmin
-        cmax = 31;
-        if (rrow >= T_kv) cmin = 32;                     // key past the end: nothing visible
-      } else {
-        cmin = 0;
-        cmax = (causal ? min(rrow + off, T_kv - 1) : T_kv - 1) - s0;
-      }
-      const bool all_visible = __all_sync(0xffffffffu, cmin <= 0 && cmax >= 31);
-      // three passes without branches inside, so the 32 columns' chains
-      // interleave: exponentials, then (diagonal tiles only) the mask, then
-      // dS and the 16-bit pairs
-      float2 pp[16];
+        // The 16-lane shape: each thread holds four keys (lanes i/4 + {0, 8,
+        // 16, 24} of the quarter) at eight of the warp's 32 columns (8r + c2
+        // and the next, r = 0..3), so it needs only those columns' lse and D
+        // (8-byte loads that four lanes share).
+        const float* v0 = reinterpret_cast<const float*>(smem + C::OFF_RING +
+                                                         slot * C::STAGE_BYTES + 2 * C::STR_BYTES) +
+                          half * 32;
+        const int c2 = 2 * (lane & 3);
+        float2 nl[4], nd[4];
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l = lv[c4];
-        const float2 x0 = __ffma2_rn(make_float2(s[4 * c4], s[4 * c4 + 1]), sl2, make_float2(-l.x, -l.y));
-        const float2 x1 =
-            __ffma2_rn(make_float2(s[4 * c4 + 2], s[4 * c4 + 3]), sl2, make_float2(-l.z, -l.w));
-        pp[2 * c4] = make_float2(ptx::ex2_approx(x0.x), ptx::ex2_approx(x0.y));
-        pp[2 * c4 + 1] = make_float2(ptx::ex2_approx(x1.x), ptx::ex2_approx(x1.y));
-      }
-      if (!all_visible) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          pp[c >> 1].x = (c >= cmin && c <= cmax) ? pp[c >> 1].x : 0.f;
-          pp[c >> 1].y = (c + 1 >= cmin && c + 1 <= cmax) ? pp[c >> 1].y : 0.f;
+        for (int r = 0; r < 4; ++r) {
+          const float2 l = *reinterpret_cast<const float2*>(v0 + 8 * r + c2);
+          const float2 d2 = *reinterpret_cast<const float2*>(v0 + kStr + 8 * r + c2);
+          nl[r] = make_float2(-l.x, -l.y);
+          nd[r] = make_float2(-d2.x, -d2.y);
         }
-      }
-      uint32_t pk[16], gk[16];
-      if constexpr (KV) {
-        // P over the first 16 columns of this warp's half of S, released at
-        // once: dV += P^T dO runs while dS is formed
+        // query s0 + c sees key x iff c >= cmin[x]
+        int cmin[4];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(pp[c].x, pp[c].y);
-        ptx::tmem_st_32x32b_x16(t_half + col_buf(b), pk);
+        for (int x = 0; x < 4; ++x) {
+          const int kx = w.r0 + quarter * 32 + 16 * (x >> 1) + (lane >> 2) + 8 * (x & 1);
+          cmin[x] = causal ? kx - off - s0 : INT_MIN / 2;
+          if (kx >= T_kv) cmin[x] = 32;  // key past the end: nothing visible
+        }
+        const bool all_visible =
+            __all_sync(0xffffffffu, max(max(cmin[0], cmin[1]), max(cmin[2], cmin[3])) <= 0);
+        // sr[16h + 4r + 2e + j] = S(key (h, e), column 8r + c2 + j); dP at +32
+        const uint32_t col = col_buf(b) + half * 32;
+        uint32_t sr[64];
+        ptx::tmem_ld_16x256b_x4(t_lane + col, *reinterpret_cast<uint32_t(*)[16]>(&sr[0]));
+        ptx::tmem_ld_16x256b_x4(t_lane + (16u << 16) + col, *reinterpret_cast<uint32_t(*)[16]>(&sr[16]));
+        ptx::tmem_ld_16x256b_x4(t_lane + col + 64, *reinterpret_cast<uint32_t(*)[16]>(&sr[32]));
+        ptx::tmem_ld_16x256b_x4(t_lane + (16u << 16) + col + 64,
+                                *reinterpret_cast<uint32_t(*)[16]>(&sr[48]));
+        tmem_wait_ld_64(sr);
+        const float* s = reinterpret_cast<const float*>(sr);
+        const float* dp = reinterpret_cast<const float*>(sr + 32);
+        float2 pp[16];  // pp[8h + 2r + e]
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 16 * h2 + 4 * r + 2 * e;
+              const float2 x = __ffma2_rn(make_float2(s[i], s[i + 1]), sl2, nl[r]);
+              pp[8 * h2 + 2 * r + e] = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+            }
+        if (!all_visible) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int c = 8 * r + c2, m = cmin[2 * h2 + e];
+                float2& v = pp[8 * h2 + 2 * r + e];
+                v.x = c >= m ? v.x : 0.f;
+                v.y = c + 1 >= m ? v.y : 0.f;
+              }
+        }
+        // P over the first 16 columns of this warp's half of S (the pair of
+        // columns 8r + c2 is word 4r + lane%4), released at once: dV += P^T dO
+        // runs while dS is formed
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) pk[j] = pack2<BF16>(pp[8 * h2 + j].x, pp[8 * h2 + j].y);
+          ptx::tmem_st_16x128b_x4(t_lane + (static_cast<uint32_t>(16 * h2) << 16) + col, pk);
+        }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&p_half[b]);
-      }
+        // dS over the first 16 columns of this warp's half of dP
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 dd = dv4[c4];
-        const float2 g0 = __fmul2_rn(pp[2 * c4], __fadd2_rn(make_float2(dp[4 * c4], dp[4 * c4 + 1]),
-                                                             make_float2(-dd.x, -dd.y)));
-        const float2 g1 = __fmul2_rn(pp[2 * c4 + 1], __fadd2_rn(make_float2(dp[4 * c4 + 2], dp[4 * c4 + 3]),
-                                                                 make_float2(-dd.z, -dd.w)));
-        gk[2 * c4] = pack2<BF16>(g0.x, g0.y);
-        gk[2 * c4 + 1] = pack2<BF16>(g1.x, g1.y);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t gk[8];
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 16 * h2 + 4 * r + 2 * e;
+              const float2 g = __fmul2_rn(pp[8 * h2 + 2 * r + e],
+                                          __fadd2_rn(make_float2(dp[i], dp[i + 1]), nd[r]));
+              gk[2 * r + e] = pack2<BF16>(g.x, g.y);
+            }
+          ptx::tmem_st_16x128b_x4(t_lane + (static_cast<uint32_t>(16 * h2) << 16) + col + 64, gk);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&p_full[b]);
+      } else {
+        uint32_t sr[64];
+        ptx::tmem_ld_32x32b_x32(t_half + col_buf(b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_ld_32x32b_x32(t_half + col_buf(b) + 64,
+                                *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_wait_ld_64(sr);
+        const float* s = reinterpret_cast<const float*>(sr);        // scores, 32 columns
+        const float* dp = reinterpret_cast<const float*>(sr + 32);  // dP, same columns
+        const float2 nl = make_float2(-l2_row, -l2_row);
+        const float2 nd = make_float2(-dd_row, -dd_row);
+        // columns [0, cmax] of this row are visible
+        const int cmax = (causal ? min(rrow + off, T_kv - 1) : T_kv - 1) - s0;
+        const bool all_visible = __all_sync(0xffffffffu, cmax >= 31);
+        float2 pp[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 x = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), sl2, nl);
+          pp[j] = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+        }
+        if (!all_visible) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            pp[c >> 1].x = c <= cmax ? pp[c >> 1].x : 0.f;
+            pp[c >> 1].y = c + 1 <= cmax ? pp[c >> 1].y : 0.f;
+          }
+        }
+        uint32_t gk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 g = __fmul2_rn(pp[j], __fadd2_rn(make_float2(dp[2 * j], dp[2 * j + 1]), nd));
+          gk[j] = pack2<BF16>(g.x, g.y);
+        }
+        // dS over the first 16 columns of this warp's half of dP
+        ptx::tmem_st_32x32b_x16(t_half + col_buf(b) + 64, gk);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&p_full[b]);
       }
-      // dS over the first 16 columns of this warp's half of dP
-      ptx::tmem_st_32x32b_x16(t_half + col_buf(b) + 64, gk);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&p_full[b]);
     }
     if (ok) {
       // -------------------------------------------------------------- epilogue
