@@ -44,6 +44,9 @@ CASES = [
     (1, 1, 640, 640, 128, F16, True),
     (1, 3, 64, 1000, 64, BF16, True),      # few rows against a long cache
     (1, 1, 5, 7, 128, BF16, False),        # tiny
+    (1, 2, 1, 300, 64, BF16, True),        # one causal query row at d = 64
+    (1, 1, 5, 7, 64, F16, False),          # tiny at d = 64
+    (1, 2, 700, 900, 64, F16, True),       # several 128-row tiles, ragged on both sides
 ]
 
 
@@ -61,6 +64,7 @@ GQA_CASES = [
     (1, 4, 2, 200, 200, 64, BF16, True),
     (2, 6, 2, 130, 257, 128, F16, False),  # group 3
     (1, 8, 1, 256, 256, 64, BF16, True),   # group 8: one CTA sums eight heads
+    (1, 8, 2, 300, 500, 64, BF16, False),  # group 4, ragged, no mask
 ]
 
 
