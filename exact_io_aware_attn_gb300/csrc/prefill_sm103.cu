@@ -1033,7 +1033,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.y = pack2<BF16>(f[2] * inv_l, f[3] * inv_l);
             v.z = pack2<BF16>(f[4] * inv_l, f[5] * inv_l);
             v.w = pack2<BF16>(f[6] * inv_l, f[7] * inv_l);
-            *reinterpret_cast<uint4*>(orow + (c * 32 + g8 * 8) * 2) = v;
+            // O is not read again by this kernel: a streaming store (evict
+            // first in L2) leaves the K/V tiles later units re-read in L2
+            __stcs(reinterpret_cast<uint4*>(orow + (c * 32 + g8 * 8) * 2), v);
           }
         }
       }
